@@ -1,0 +1,516 @@
+"""Benchmark of the fused residual-add + RMSNorm + FP8 / NVFP4 / MXFP4 path on GB300.
+
+One step is one pass of the whole hot path over one batch: the three quantisation modes, each on
+its own resident [8192 x 4096] bf16 batch with a residual (the fp8_residual workload's shape and
+distributions; FP8 with scale_ub 1200, NVFP4 with a device-computed global scale, MXFP4), so a
+step reads 384 MiB of inputs -- more than the 129 MB L2 -- and every launch streams from HBM.
+
+Prints one JSON line:
+  value     whole-job GB/s of algorithmic bytes (each launch's reads + writes counted once),
+            inputs resident in HBM, CUDA-event timed over exactly K steps
+  e2e       the same metric through the public API with host buffers: pinned host -> device
+            copies of the step's inputs and device -> host copies of its outputs inside the
+            timed region
+  roofline  the dominant kernel's achieved GB/s (its algorithmic bytes / its average launch time,
+            events on its launching stream) against the measured HBM copy bandwidth
+  cpu_baseline  the oracle on a bounded sample of the same workload, on this host's cores
+
+--impl reference times the oracle itself as the reference arm. --report runs every workload
+(fp8_small ... the MXFP4 sweep) and prints one JSON line per workload with its GB/s.
+Multi-GPU (torchrun): every rank runs an independent replica (the path has no exchange step);
+value is the sum of all ranks' bytes over the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+import workloads as W  # noqa: E402
+
+METRIC = "achieved HBM GB/s & rows/s, fused RMSNorm+FP8/FP4 quant, % of GB300 8 TB/s"
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+STEP_SHAPE = (8192, 4096)
+MODES = ("fp8", "nvfp4", "mxfp4")
+
+
+# ------------------------------------------------------------------------------------------
+# helpers
+# ------------------------------------------------------------------------------------------
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_sha():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "rmsnorm_precision_activation_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel):
+    """Per-launch DRAM bytes of `kernel` from the committed ncu summary, if it was taken on the
+    current kernel sources; else None."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+    except Exception:
+        return None
+    if d.get("source_sha") != kernel_source_sha():
+        return None
+    e = d.get("kernels", {}).get(kernel)
+    return None if e is None else e.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except Exception:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in getattr(self, "lines", []):
+            f = [x.strip() for x in l.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def mode_bytes(mode, rows, hidden, residual=True):
+    name = {"fp8": "fp8_residual", "nvfp4": "nvfp4", "mxfp4": "mxfp4_residual"}[mode]
+    return W.Workload(name, mode, rows, hidden, "bf16", residual).algorithmic_bytes()
+
+
+# ------------------------------------------------------------------------------------------
+# our arm
+# ------------------------------------------------------------------------------------------
+
+class Step:
+    """Resident buffers for one step: one batch per mode, outputs, and the launches."""
+
+    def __init__(self, rq, rows, hidden, device, seed=0):
+        self.rq = rq
+        self.rows, self.hidden = rows, hidden
+        base = W.config("fp8_residual", rows=rows, hidden=hidden)
+        self.batches = {}
+        for k, mode in enumerate(MODES):
+            d = W.generate(base, seed=seed + k, device=device)
+            self.batches[mode] = d
+        self.w = base
+        dev = device
+        self.out = {
+            "fp8": (torch.empty(rows, hidden, dtype=torch.float8_e4m3fn, device=dev),
+                    torch.empty(rows, dtype=torch.float32, device=dev),
+                    torch.empty(rows, hidden, dtype=torch.bfloat16, device=dev)),
+            "nvfp4": (torch.empty(rows, hidden // 2, dtype=torch.uint8, device=dev),
+                      torch.empty(rows, hidden // 16, dtype=torch.float8_e4m3fn, device=dev),
+                      torch.empty(rows, hidden, dtype=torch.bfloat16, device=dev)),
+            "mxfp4": (torch.empty(rows, hidden // 2, dtype=torch.uint8, device=dev),
+                      torch.empty(rows, hidden // 32, dtype=torch.uint8, device=dev),
+                      torch.empty(rows, hidden, dtype=torch.bfloat16, device=dev)),
+        }
+        nb = self.batches["nvfp4"]
+        self.gs = rq.rmsnorm_nvfp4_global_scale(nb["input"], nb["gamma"], residual=nb["residual"],
+                                                epsilon=base.eps)
+        self.bytes = {m: mode_bytes(m, rows, hidden) for m in MODES}
+        self.step_bytes = sum(self.bytes.values())
+
+    def launch(self, mode, stream=None):
+        d, o, w, rq = self.batches[mode], self.out[mode], self.w, self.rq
+        if mode == "fp8":
+            rq.rmsnorm_quant_fp8(d["input"], d["gamma"], residual=d["residual"], residual_output=o[2],
+                                 epsilon=w.eps, weight_offset=w.weight_offset, scale_ub=w.scale_ub,
+                                 output=o[0], scale_output=o[1], stream=stream)
+        elif mode == "nvfp4":
+            rq.rmsnorm_quant_nvfp4(d["input"], d["gamma"], global_scale=self.gs,
+                                   residual=d["residual"], residual_output=o[2], epsilon=w.eps,
+                                   output=o[0], block_scale=o[1], stream=stream)
+        else:
+            rq.rmsnorm_quant_mxfp4(d["input"], d["gamma"], residual=d["residual"],
+                                   residual_output=o[2], epsilon=w.eps, output=o[0],
+                                   block_scale=o[1], stream=stream)
+
+
+def barrier_max(value, world):
+    if world == 1:
+        return value
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def run_ours(args):
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    from rmsnorm_precision_activation_gb300 import build as B
+    B.build()
+    import rmsnorm_precision_activation_gb300 as rq
+
+    device = torch.device("cuda", local)
+    rows, hidden = STEP_SHAPE
+    step = Step(rq, rows, hidden, device)
+    stream = torch.cuda.current_stream(device)
+
+    for _ in range(args.warmup):
+        for m in MODES:
+            step.launch(m)
+    torch.cuda.synchronize()
+
+    K = args.steps
+    ev = {m: [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(K)] for m in MODES}
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    launches0 = rq.rmsq_launch_count()
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clocks:
+        t0.record(stream)
+        for i in range(K):
+            for m in MODES:
+                ev[m][i][0].record(stream)
+                step.launch(m)
+                ev[m][i][1].record(stream)
+        t1.record(stream)
+        torch.cuda.synchronize()
+    barrier(world)
+    launches = rq.rmsq_launch_count() - launches0
+    total_ms = barrier_max(t0.elapsed_time(t1), world)
+    per_mode_ms = {m: statistics.mean(a.elapsed_time(b) for a, b in ev[m]) for m in MODES}
+    assert rq.rmsq_device_status() == 0
+
+    # ---- end to end through the public API with host buffers -------------------------------
+    e2e = run_e2e(rq, step, device, max(3, min(K, 10)), world)
+
+    bytes_all = step.step_bytes * K * world
+    value = bytes_all / (total_ms * 1e-3) / 1e9
+    rows_per_s = 3 * rows * K * world / (total_ms * 1e-3)
+    dom = max(per_mode_ms, key=per_mode_ms.get)
+    dom_gbs = step.bytes[dom] / (per_mode_ms[dom] * 1e-3) / 1e9
+    peak, peak_src = measured_peak()
+    kname = {"fp8": "rmsnorm_quant_fp8", "nvfp4": "rmsnorm_quant_nvfp4",
+             "mxfp4": "rmsnorm_quant_mxfp4"}[dom]
+    line = {
+        "metric": METRIC,
+        "value": round(value, 1),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": K,
+        "warmup": args.warmup,
+        "ms_per_step": round(total_ms / K, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32",
+        "data": "synthetic (seeded; workload fp8_residual distributions)",
+        "config": {
+            "workload": "fused residual-add + RMSNorm + {FP8 per-row, NVFP4, MXFP4} quantisation, "
+                        "one [8192 x 4096] bf16 batch with residual per mode",
+            "rows": rows, "hidden": hidden, "io_dtype": "bf16", "residual": True,
+            "modes": list(MODES), "fp8_scale_ub": 1200.0, "nvfp4_global_scale": "device pre-pass",
+            "l2": "inputs larger than L2: %d MiB of distinct inputs per step, no flush"
+                  % (3 * 2 * rows * hidden * 2 // (1 << 20)),
+            "parallelism": "replicas" if world > 1 else "single GPU",
+        },
+        "rows_per_s": round(rows_per_s),
+        "pct_of_8tbs": round(100 * value / world / NOMINAL_HBM_GBS, 2),
+        "per_mode": {m: {"us": round(per_mode_ms[m] * 1e3, 2),
+                         "gbs": round(step.bytes[m] / (per_mode_ms[m] * 1e-3) / 1e9, 1),
+                         "algorithmic_bytes": step.bytes[m]} for m in MODES},
+        "roofline": {"bound": "hbm", "kernel": kname, "achieved": round(dom_gbs, 1),
+                     "peak": peak, "peak_source": peak_src + " (MEASURED_PEAKS hbm_gbs, copy)",
+                     "unit": "GB/s", "frac": round(dom_gbs / peak, 4),
+                     "traffic": recorded_traffic(kname),
+                     "algorithmic_bytes_per_launch": step.bytes[dom]},
+        "e2e": e2e,
+        "gpu_launches": int(launches),
+        "clocks": clocks.summary(),
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(seconds=args.cpu_seconds)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def run_e2e(rq, step, device, K, world):
+    """Same step through the public API, inputs from pinned host memory and outputs back to
+    pinned host memory inside the timed region."""
+    host_in = {m: {k: v.cpu().pin_memory() for k, v in step.batches[m].items() if v is not None}
+               for m in MODES}
+    host_out = {m: tuple(torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in step.out[m])
+                for m in MODES}
+    h2d = sum(t.numel() * t.element_size() for d in host_in.values() for t in d.values())
+    d2h = sum(t.numel() * t.element_size() for o in host_out.values() for t in o)
+    stream = torch.cuda.current_stream(device)
+
+    def one():
+        for m in MODES:
+            for k, t in host_in[m].items():
+                step.batches[m][k].copy_(t, non_blocking=True)
+            step.launch(m)
+            for dst, src in zip(host_out[m], step.out[m]):
+                dst.copy_(src, non_blocking=True)
+
+    one()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    a.record(stream)
+    for _ in range(K):
+        one()
+    b.record(stream)
+    torch.cuda.synchronize()
+    ms = barrier_max(a.elapsed_time(b), world)
+    return {"value": round(step.step_bytes * K * world / (ms * 1e-3) / 1e9, 1), "unit": "GB/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "ms_per_step": round(ms / K, 4), "steps": K}
+
+
+# ------------------------------------------------------------------------------------------
+# the oracle on the host cores
+# ------------------------------------------------------------------------------------------
+
+def oracle_sample(rows_per_mode, seed=0):
+    import numpy as np
+    import oracle
+    rows, hidden = rows_per_mode, STEP_SHAPE[1]
+    base = W.config("fp8_residual", rows=rows, hidden=hidden)
+    data = {}
+    for k, m in enumerate(MODES):
+        d = W.generate(base, seed=seed + k)
+        data[m] = tuple(W.bits(d[n]) for n in ("input", "residual", "gamma"))
+    x, r, g = data["nvfp4"]
+    y = oracle.rmsnorm(x, r, g, eps=base.eps)["y"]
+    gs = float(oracle.nvfp4_global_scale(np.abs(y).max()))
+
+    def run(threads=None):
+        x, r, g = data["fp8"]
+        oracle.quant_fp8(x, r, g, eps=base.eps, scale_ub=base.scale_ub, threads=threads)
+        x, r, g = data["nvfp4"]
+        oracle.quant_nvfp4(x, r, g, gs, eps=base.eps, threads=threads)
+        x, r, g = data["mxfp4"]
+        oracle.quant_mxfp4(x, r, g, eps=base.eps, threads=threads)
+
+    nbytes = sum(mode_bytes(m, rows, hidden) for m in MODES)
+    return run, nbytes
+
+
+def cpu_baseline(seconds=15.0):
+    import oracle
+    oracle.build()
+    cores = oracle.cores()
+    probe_rows = 64
+    run, nb = oracle_sample(probe_rows)
+    t = time.perf_counter()
+    run()
+    dt = max(time.perf_counter() - t, 1e-3)
+    rows = int(max(probe_rows, min(8192, probe_rows * seconds / dt / 2)))
+    run, nb = oracle_sample(rows, seed=100)
+    t = time.perf_counter()
+    run()
+    dt = time.perf_counter() - t
+    return {"value": round(nb / dt / 1e9, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "sample": "%d rows x 4096 per mode (fp8 / nvfp4 / mxfp4, bf16 + residual), %.1f s"
+                      % (rows, dt),
+            "rows_per_s": round(3 * rows / dt, 1)}
+
+
+def run_reference(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    cores = oracle.cores()
+    budget = 120.0 / max(1, args.steps + args.warmup)      # whole run within ~2 minutes
+    run, nb = oracle_sample(64)
+    t = time.perf_counter()
+    run()
+    dt = max(time.perf_counter() - t, 1e-3)
+    rows = int(max(16, min(8192, 64 * budget / dt / 2)))
+    run, nb = oracle_sample(rows, seed=200)
+    for _ in range(args.warmup):
+        run()
+    times = []
+    for _ in range(args.steps):
+        t = time.perf_counter()
+        run()
+        times.append(time.perf_counter() - t)
+    total = sum(times)
+    value = nb * args.steps / total / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(total / args.steps * 1e3, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded; workload fp8_residual distributions)",
+        "config": {"workload": "fused residual-add + RMSNorm + {FP8 per-row, NVFP4, MXFP4} "
+                               "quantisation, one [8192 x 4096] bf16 batch with residual per mode",
+                   "rows": STEP_SHAPE[0], "hidden": STEP_SHAPE[1], "io_dtype": "bf16",
+                   "residual": True, "modes": list(MODES),
+                   "sample_rows_per_mode": rows},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": cores,
+                         "kind": "oracle",
+                         "sample": "%d of 8192 rows per mode per step" % rows},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------------------------------
+# per-workload report
+# ------------------------------------------------------------------------------------------
+
+def report_workloads():
+    names = [("fp8_small", None, None), ("fp8_residual", None, None), ("fp8_gemma", None, None),
+             ("nvfp4", None, None)]
+    names += [("mxfp4_residual", r, h) for r in W.MXFP4_ROWS for h in W.MXFP4_HIDDEN]
+    return names
+
+
+def run_report(args):
+    from rmsnorm_precision_activation_gb300 import build as B
+    B.build()
+    import rmsnorm_precision_activation_gb300 as rq
+    torch.cuda.set_device(0)
+    peak, _ = measured_peak()
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    for name, rows, hidden in report_workloads():
+        w = W.config(name, rows=rows, hidden=hidden)
+        d = W.generate(w, seed=0, device="cuda")
+        x, r, g = d["input"], d["residual"], d["gamma"]
+        if w.mode == "fp8":
+            fn = lambda: rq.rmsnorm_quant_fp8(x, g, residual=r, epsilon=w.eps,
+                                              weight_offset=w.weight_offset, scale_ub=w.scale_ub)
+        elif w.mode == "nvfp4":
+            gs = rq.rmsnorm_nvfp4_global_scale(x, g, residual=r, epsilon=w.eps)
+            fn = lambda: rq.rmsnorm_quant_nvfp4(x, g, global_scale=gs, residual=r, epsilon=w.eps)
+        else:
+            fn = lambda: rq.rmsnorm_quant_mxfp4(x, g, residual=r, epsilon=w.eps)
+        outs = fn()        # warm + allocate
+        for _ in range(3):
+            fn()
+        times = []
+        for _ in range(args.report_reps):
+            flush.fill_(1)                      # evict L2 between repetitions
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            fn()
+            b.record()
+            b.synchronize()
+            times.append(a.elapsed_time(b))
+        us = statistics.median(times) * 1e3
+        gbs = w.algorithmic_bytes() / (us * 1e-6) / 1e9
+        print(json.dumps({"workload": name, "shape": [w.rows, w.hidden], "io_dtype": w.dtype,
+                          "mode": w.mode, "residual": w.residual, "us": round(us, 2),
+                          "algorithmic_bytes": w.algorithmic_bytes(), "gbs": round(gbs, 1),
+                          "rows_per_s": round(w.rows / (us * 1e-6)),
+                          "frac_of_measured": round(gbs / peak, 4),
+                          "pct_of_8tbs": round(100 * gbs / NOMINAL_HBM_GBS, 2)}), flush=True)
+        del outs, d
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--report", action="store_true", help="per-workload GB/s lines")
+    ap.add_argument("--report-reps", type=int, default=20)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)       # at least 3 untimed warm-up steps, always
+    if args.impl == "reference":
+        run_reference(args)
+    elif args.report:
+        run_report(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -74,7 +74,7 @@ def _load():
                  "oracle_bf16_round_array", "oracle_fp16_round_array", "oracle_ue8m0_code_array"):
         getattr(lib, name).argtypes = [P, P, I64]
         getattr(lib, name).restype = None
-    lib.oracle_quant_fp8.argtypes = [P, P, I, P, I64, I64, F, F, F, P, P, P, P, P, P]
+    lib.oracle_quant_fp8.argtypes = [P, P, I, P, I64, I64, F, F, F, I, P, P, P, P, P, P]
     lib.oracle_quant_nvfp4.argtypes = [P, P, I, P, I64, I64, F, F, F, I, P, P, P, P, P, P, P]
     lib.oracle_quant_mxfp4.argtypes = [P, P, I, P, I64, I64, F, F, I, P, P, P, P, P, P, P]
     lib.oracle_rmsnorm.argtypes = [P, P, I, P, I64, I64, F, F, P, P, P]
@@ -222,10 +222,11 @@ class _Rows:
 
 
 def quant_fp8(x, residual, gamma, *, dtype=BF16, eps=1e-6, weight_offset=0.0, scale_ub=1200.0,
-              want_y=False, want_pre=False, threads=None):
+              scale_dtype=F32, want_y=False, want_pre=False, threads=None):
     """FP8 E4M3 with a per-row dynamic scale. Inputs are bit arrays [rows, H] (uint16 for bf16 /
-    fp16, float32 for fp32). Returns a dict with q [rows, H] uint8, scale [rows] float32,
-    residual_output (or None), and optionally y (float32) and pre (float64, y / scale)."""
+    fp16, float32 for fp32). Returns a dict with q [rows, H] uint8, scale [rows] float32 (the
+    stored scale, rounded to scale_dtype and widened), residual_output (or None), and optionally
+    y (float32) and pre (float64, y / scale)."""
     lib = _load()
     x, residual, gamma = _as_input(x, dtype), _as_input(residual, dtype), _as_input(gamma, dtype)
     rows, H = x.shape
@@ -242,7 +243,8 @@ def quant_fp8(x, residual, gamma, *, dtype=BF16, eps=1e-6, weight_offset=0.0, sc
             return
         tmp = np.zeros(H, np.float32)
         lib.oracle_quant_fp8(R[0].at(r0), R[1].at(r0), dtype, _ptr(gamma), r1 - r0, H, eps,
-                             weight_offset, scale_ub, R[2].at(r0), R[3].at(r0), scale_rows.at(r0),
+                             weight_offset, scale_ub, scale_dtype, R[2].at(r0), R[3].at(r0),
+                             scale_rows.at(r0),
                              R[4].at(r0), R[5].at(r0), _ptr(tmp))
 
     _run_rows(run, rows, threads)

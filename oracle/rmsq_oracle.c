@@ -255,11 +255,14 @@ static float row_front(const void* x, const void* res, int dtype, const void* ga
 
 /* FP8 per-row dynamic quantisation ([rms_norm_fused_fp8], [allreduce_fp8]):
  *   amax = max_i |y_i|;  scale = RN_fp32(min(amax, scale_ub) / 448);  q_i = E4M3(y_i / scale),
- *   with q = 0 on a row whose scale is 0. */
+ *   with q = 0 on a row whose scale is 0.
+ * [rms_norm_fused_fp8] lets the scale be stored as bf16 or fp16 (parameter scales_dtype): the fp32
+ * scale is then rounded to that type, and the codes are formed against the stored value so that
+ * y ~= dec(q) * stored scale. scale_out receives the stored value widened to fp32. */
 int oracle_quant_fp8(const void* input, const void* residual, int dtype, const void* gamma,
                      int64_t rows, int64_t hidden, float eps, float weight_offset, float scale_ub,
-                     void* residual_output, uint8_t* q, float* scale_out, float* y_out,
-                     double* pre_out, float* y_tmp)
+                     int scale_dtype, void* residual_output, uint8_t* q, float* scale_out,
+                     float* y_out, double* pre_out, float* y_tmp)
 {
     size_t esz = dtype == ORACLE_F32 ? 4 : 2;
     for (int64_t r = 0; r < rows; r++) {
@@ -273,6 +276,10 @@ int oracle_quant_fp8(const void* input, const void* residual, int dtype, const v
             if (fabsf(y[i]) > amax) amax = fabsf(y[i]);
         double clamped = amax < scale_ub ? amax : scale_ub;
         float scale = (float)(clamped / 448.0);
+        if (scale_dtype == ORACLE_BF16)
+            scale = (float)oracle_bf16_to_double(oracle_double_to_bf16(scale));
+        else if (scale_dtype == ORACLE_FP16)
+            scale = (float)oracle_fp16_to_double(oracle_double_to_fp16(scale));
         scale_out[r] = scale;
         for (int64_t i = 0; i < hidden; i++) {
             double v = scale > 0.0f ? (double)y[i] / (double)scale : 0.0;

@@ -1,0 +1,473 @@
+// rmsq_api.cu -- the C ABI of librmsq.so: argument checks, launch planning, the entry points
+// declared in include/rmsq.h, and a few small diagnostic kernels.
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "rmsq.h"
+#include "rmsq_host.h"
+
+namespace rmsq {
+
+// Device-side error word (bit ERRF_WAIT_TIMEOUT: a bounded wait ran out). One per device.
+static __device__ unsigned int g_err_word;
+
+static std::atomic<int> g_schedule{0};
+static std::atomic<int> g_tune_stages{0};
+static std::atomic<int> g_tune_ctas{0};
+static std::atomic<int> g_tune_vpt{0};
+static std::atomic<unsigned long long> g_timeout_ns{2000000000ull};
+static std::atomic<unsigned long long> g_launches{0};
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceInfo {
+    bool ready = false;
+    bool usable = false;
+    int sms = 0;
+    int smem_optin = 0;
+    unsigned int* err = nullptr;
+};
+
+static std::mutex g_mu;
+static DeviceInfo g_dev[kMaxDevices];
+
+// Per-device facts, read once with the device current: SM count, opt-in shared memory, the
+// address of this device's error word, and whether the device is compute capability 10.3.
+static const DeviceInfo* device_info()
+{
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+        cudaGetLastError();
+        return nullptr;
+    }
+    std::lock_guard<std::mutex> lock(g_mu);
+    DeviceInfo& d = g_dev[dev];
+    if (!d.ready) {
+        int major = 0, minor = 0;
+        bool ok = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) == cudaSuccess &&
+                  cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) == cudaSuccess &&
+                  cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess &&
+                  cudaDeviceGetAttribute(&d.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) ==
+                      cudaSuccess;
+        void* addr = nullptr;
+        ok = ok && major == 10 && minor == 3 &&
+             cudaGetSymbolAddress(&addr, g_err_word) == cudaSuccess;
+        d.err = static_cast<unsigned int*>(addr);
+        d.usable = ok;
+        d.ready = true;
+        if (!ok) cudaGetLastError();
+    }
+    return d.usable ? &d : nullptr;
+}
+
+struct OccEntry {
+    const void* fn;
+    int dev, threads, smem, blocks;
+    bool attr_set;
+};
+static OccEntry g_occ[512];
+static int g_nocc = 0;
+
+cudaError_t run_kernel(const void* fn, const Plan& pl, const Params& p, cudaStream_t stream)
+{
+    int dev = 0;
+    cudaGetDevice(&dev);
+    const DeviceInfo& di = g_dev[dev];
+    int blocks = 0;
+    {
+        std::lock_guard<std::mutex> lock(g_mu);
+        int i = 0;
+        for (; i < g_nocc; ++i)
+            if (g_occ[i].fn == fn && g_occ[i].dev == dev && g_occ[i].threads == pl.threads &&
+                g_occ[i].smem == pl.smem)
+                break;
+        if (i == g_nocc) {
+            cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 di.smem_optin);
+            if (e != cudaSuccess) return e;
+            int b = 0;
+            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, fn, pl.threads, pl.smem);
+            if (e != cudaSuccess) return e;
+            if (g_nocc < static_cast<int>(sizeof(g_occ) / sizeof(g_occ[0])))
+                g_occ[g_nocc++] = OccEntry{fn, dev, pl.threads, pl.smem, b, true};
+            blocks = b;
+        } else {
+            blocks = g_occ[i].blocks;
+        }
+    }
+    if (blocks < 1) return cudaErrorInvalidConfiguration;
+    if (pl.ctas_per_sm > 0 && blocks > pl.ctas_per_sm) blocks = pl.ctas_per_sm;
+    long long grid = static_cast<long long>(blocks) * di.sms;
+    if (grid > p.rows) grid = p.rows;
+    void* args[] = {const_cast<Params*>(&p)};
+    cudaError_t e = cudaLaunchKernel(fn, dim3(static_cast<unsigned>(grid)), dim3(pl.threads), args,
+                                     static_cast<size_t>(pl.smem), stream);
+    if (e == cudaSuccess) g_launches.fetch_add(1, std::memory_order_relaxed);
+    return e;
+}
+
+// ------------------------------------------------------------------------------------------
+// Planning
+// ------------------------------------------------------------------------------------------
+
+static int elems_per_vec(int dt) { return dt == DT_F32 ? 4 : 8; }
+
+// Pick vectors per thread, CTA size, schedule, ring depth and residency for one call.
+// Measured on GB300: small CTAs (about 128 threads, 4 vectors of 16 bytes each per thread per
+// row), a two-row ring each, and as many CTAs per SM as shared memory and registers allow keep
+// several rows in computation per SM while the next ones stream in.
+static bool make_plan(int mode, int dt, bool res, int hidden, const DeviceInfo& di, Plan& pl)
+{
+    const int nv = hidden / elems_per_vec(dt);
+    pl.mode = mode;
+    pl.dt = dt;
+    pl.res = res;
+    int vpt = g_tune_vpt.load();
+    if (vpt == 0) {
+        vpt = 4;
+        while (vpt < 8 && (nv + vpt - 1) / vpt > 512) vpt *= 2;
+        while (vpt > 1 && (nv + vpt - 1) / vpt < 64) vpt /= 2;
+    }
+    int threads = ((nv + vpt - 1) / vpt + 31) / 32 * 32;
+    if (threads > 512) return false;
+    pl.vpt = vpt;
+    pl.threads = threads;
+
+    const int red_bytes = kRedFloats * 4;
+    const long long stage = static_cast<long long>(nv) * 16 * (res ? 2 : 1);
+    const int forced = g_schedule.load();
+    const bool pipe_fits = 2 * stage + red_bytes + 2 * 8 <= di.smem_optin;
+    pl.sched = (forced == SCHED_REG || !pipe_fits) ? SCHED_REG : SCHED_PIPE;
+    pl.ctas_per_sm = g_tune_ctas.load();
+    if (pl.ctas_per_sm == 0) pl.ctas_per_sm = 16;
+    if (pl.sched == SCHED_PIPE) {
+        int stages = g_tune_stages.load();
+        if (stages == 0) stages = 2;
+        while (stages > 2 && stages * stage + red_bytes + stages * 8 > di.smem_optin) --stages;
+        pl.stages = stages;
+        pl.smem = static_cast<int>(stages * stage) + red_bytes + stages * 8;
+    } else {
+        pl.stages = 0;
+        pl.smem = red_bytes;
+    }
+    return true;
+}
+
+static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Checks shared by every entry point. Returns RMSQ_OK with *empty set for a valid rows == 0
+// call, whose data pointers are not examined.
+static rmsq_status check_common(const void* input, const void* residual, const void* residual_output,
+                                const void* gamma, int64_t rows, int64_t hidden, int dtype,
+                                float epsilon, float weight_offset, int min_multiple, bool* empty)
+{
+    *empty = false;
+    if (dtype != RMSQ_BF16 && dtype != RMSQ_FP16 && dtype != RMSQ_F32) return RMSQ_ERR_DTYPE;
+    const int64_t max_h = dtype == RMSQ_F32 ? RMSQ_MAX_HIDDEN / 2 : RMSQ_MAX_HIDDEN;
+    if (rows < 0 || hidden < min_multiple || hidden > max_h || hidden % min_multiple != 0)
+        return RMSQ_ERR_SHAPE;
+    if (!(epsilon >= 0.0f) || !std::isfinite(epsilon) || !std::isfinite(weight_offset))
+        return RMSQ_ERR_VALUE;
+    if (rows == 0) {
+        *empty = true;
+        return RMSQ_OK;
+    }
+    if (!input || !gamma) return RMSQ_ERR_NULL;
+    if ((residual == nullptr) != (residual_output == nullptr)) return RMSQ_ERR_NULL;
+    if (!aligned16(input) || !aligned16(gamma) || !aligned16(residual) || !aligned16(residual_output))
+        return RMSQ_ERR_ALIGN;
+    return RMSQ_OK;
+}
+
+static Params base_params(const void* input, const void* residual, void* residual_output,
+                          const void* gamma, int64_t rows, int64_t hidden, int dtype, float epsilon,
+                          float weight_offset, const DeviceInfo& di)
+{
+    Params p;
+    std::memset(&p, 0, sizeof p);
+    p.x = input;
+    p.res = residual;
+    p.res_out = residual_output;
+    p.gamma = gamma;
+    p.err = di.err;
+    p.rows = rows;
+    p.hidden = static_cast<int>(hidden);
+    p.nvec = static_cast<int>(hidden / elems_per_vec(dtype));
+    p.eps = epsilon;
+    p.offset = weight_offset;
+    p.timeout_ns = g_timeout_ns.load();
+    return p;
+}
+
+static rmsq_status launch(int mode, Params& p, bool res, int dtype, const DeviceInfo& di,
+                          cudaStream_t stream)
+{
+    Plan pl;
+    if (!make_plan(mode, dtype, res, p.hidden, di, pl)) return RMSQ_ERR_SHAPE;
+    p.stages = pl.stages;
+    cudaError_t e;
+    switch (mode) {
+    case MODE_FP8: e = dispatch_fp8(pl, p, stream); break;
+    case MODE_NVFP4: e = dispatch_nvfp4(pl, p, stream); break;
+    case MODE_MXFP4: e = dispatch_mxfp4(pl, p, stream); break;
+    default: e = dispatch_amax(pl, p, stream); break;
+    }
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return RMSQ_ERR_LAUNCH;
+    }
+    return RMSQ_OK;
+}
+
+// ------------------------------------------------------------------------------------------
+// Diagnostic kernels
+// ------------------------------------------------------------------------------------------
+
+__global__ void selftest_wait_kernel(unsigned int* err, unsigned long long timeout_ns)
+{
+    __shared__ __align__(8) uint64_t bar;
+    if (threadIdx.x == 0) {
+        mbar_init(smem_u32(&bar), 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
+    // Nothing arrives on this barrier: the wait must run out and report it.
+    const bool ok = mbar_wait_bounded(smem_u32(&bar), 0, timeout_ns);
+    if (__syncthreads_or(!ok) && threadIdx.x == 0) atomicOr(err, ERRF_WAIT_TIMEOUT);
+}
+
+__global__ void debug_convert_kernel(int fmt, const float* __restrict__ in,
+                                     unsigned char* __restrict__ out, long long n)
+{
+    for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < n;
+         i += static_cast<long long>(gridDim.x) * blockDim.x) {
+        const float v = in[i];
+        if (fmt == 0) {
+            out[i] = static_cast<unsigned char>(cvt_e4m3x2(v, 0.0f) & 0xFFu);
+        } else {
+            const float q[4] = {v, 0.0f, 0.0f, 0.0f};
+            out[i] = static_cast<unsigned char>(cvt_e2m1x4(q) & 0xFu);
+        }
+    }
+}
+
+// gs = 448 * 6 / amax, where *gs holds amax's bits on entry; an all-zero tensor gives gs = 1.
+__global__ void finalize_global_scale_kernel(float* gs)
+{
+    const float amax = __uint_as_float(*reinterpret_cast<unsigned int*>(gs));
+    *gs = amax > 0.0f ? __fdiv_rn(448.0f * 6.0f, amax) : 1.0f;
+}
+
+}  // namespace rmsq
+
+using namespace rmsq;
+
+// ------------------------------------------------------------------------------------------
+// C ABI
+// ------------------------------------------------------------------------------------------
+
+extern "C" rmsq_status rmsnorm_quant_fp8(const void* input, const void* residual,
+                                         void* residual_output, const void* gamma, int64_t rows,
+                                         int64_t hidden, int dtype, float epsilon,
+                                         float weight_offset, float scale_ub, void* output,
+                                         void* scale_output, int scale_dtype, void* stream)
+{
+    bool empty;
+    rmsq_status st = check_common(input, residual, residual_output, gamma, rows, hidden, dtype,
+                                  epsilon, weight_offset, dtype == RMSQ_F32 ? 4 : 8, &empty);
+    if (st != RMSQ_OK) return st;
+    if (scale_dtype != RMSQ_F32 && scale_dtype != RMSQ_BF16 && scale_dtype != RMSQ_FP16)
+        return RMSQ_ERR_DTYPE;
+    if (!(scale_ub > 0.0f)) return RMSQ_ERR_VALUE;
+    if (empty) return RMSQ_OK;
+    if (!output || !scale_output) return RMSQ_ERR_NULL;
+    if (!aligned16(output) || !aligned16(scale_output)) return RMSQ_ERR_ALIGN;
+    const DeviceInfo* di = device_info();
+    if (!di) return RMSQ_ERR_DEVICE;
+    Params p = base_params(input, residual, residual_output, gamma, rows, hidden, dtype, epsilon,
+                           weight_offset, *di);
+    p.out = output;
+    p.scale_out = scale_output;
+    p.scale_ub = scale_ub;
+    p.scale_dtype = scale_dtype;
+    return launch(MODE_FP8, p, residual != nullptr, dtype, *di, static_cast<cudaStream_t>(stream));
+}
+
+static rmsq_status fp4_common(int mode, const void* input, const void* residual,
+                              void* residual_output, const void* gamma, int64_t rows,
+                              int64_t hidden, int dtype, float epsilon, float weight_offset,
+                              const float* global_scale, void* output, void* block_scale,
+                              int scale_layout, void* stream)
+{
+    const int block = mode == MODE_NVFP4 ? 16 : 32;
+    bool empty;
+    rmsq_status st = check_common(input, residual, residual_output, gamma, rows, hidden, dtype,
+                                  epsilon, weight_offset, block, &empty);
+    if (st != RMSQ_OK) return st;
+    if (scale_layout != RMSQ_SCALE_ROW_MAJOR && scale_layout != RMSQ_SCALE_SWIZZLED_128x4)
+        return RMSQ_ERR_DTYPE;
+    if (empty) return RMSQ_OK;
+    if (!output || !block_scale) return RMSQ_ERR_NULL;
+    if (mode == MODE_NVFP4 && !global_scale) return RMSQ_ERR_NULL;
+    if (!aligned16(output) || !aligned16(block_scale)) return RMSQ_ERR_ALIGN;
+    if (mode == MODE_NVFP4 && (reinterpret_cast<uintptr_t>(global_scale) & 3u)) return RMSQ_ERR_ALIGN;
+    const DeviceInfo* di = device_info();
+    if (!di) return RMSQ_ERR_DEVICE;
+    Params p = base_params(input, residual, residual_output, gamma, rows, hidden, dtype, epsilon,
+                           weight_offset, *di);
+    p.out = output;
+    p.scale_out = block_scale;
+    p.gs = global_scale;
+    p.swizzled = scale_layout == RMSQ_SCALE_SWIZZLED_128x4;
+    p.nsf = static_cast<int>(hidden / block);
+    p.k_tiles = (p.nsf + 3) / 4;
+    return launch(mode, p, residual != nullptr, dtype, *di, static_cast<cudaStream_t>(stream));
+}
+
+extern "C" rmsq_status rmsnorm_quant_nvfp4(const void* input, const void* residual,
+                                           void* residual_output, const void* gamma, int64_t rows,
+                                           int64_t hidden, int dtype, float epsilon,
+                                           float weight_offset, const float* global_scale,
+                                           void* output, void* block_scale, int scale_layout,
+                                           void* stream)
+{
+    return fp4_common(MODE_NVFP4, input, residual, residual_output, gamma, rows, hidden, dtype,
+                      epsilon, weight_offset, global_scale, output, block_scale, scale_layout,
+                      stream);
+}
+
+extern "C" rmsq_status rmsnorm_quant_mxfp4(const void* input, const void* residual,
+                                           void* residual_output, const void* gamma, int64_t rows,
+                                           int64_t hidden, int dtype, float epsilon,
+                                           float weight_offset, void* output, void* block_scale,
+                                           int scale_layout, void* stream)
+{
+    return fp4_common(MODE_MXFP4, input, residual, residual_output, gamma, rows, hidden, dtype,
+                      epsilon, weight_offset, nullptr, output, block_scale, scale_layout, stream);
+}
+
+extern "C" rmsq_status rmsnorm_nvfp4_global_scale(const void* input, const void* residual,
+                                                  const void* gamma, int64_t rows, int64_t hidden,
+                                                  int dtype, float epsilon, float weight_offset,
+                                                  float* gs_out, void* stream)
+{
+    if (!gs_out) return RMSQ_ERR_NULL;
+    // the residual is read but no residual_output is written: pass it as its own pair partner
+    bool empty;
+    rmsq_status st = check_common(input, residual, residual, gamma, rows, hidden, dtype, epsilon,
+                                  weight_offset, 16, &empty);
+    if (st != RMSQ_OK) return st;
+    if (reinterpret_cast<uintptr_t>(gs_out) & 3u) return RMSQ_ERR_ALIGN;
+    const DeviceInfo* di = device_info();
+    if (!di) return RMSQ_ERR_DEVICE;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (cudaMemsetAsync(gs_out, 0, sizeof(float), s) != cudaSuccess) {
+        cudaGetLastError();
+        return RMSQ_ERR_LAUNCH;
+    }
+    if (rows > 0) {
+        Params p = base_params(input, residual, nullptr, gamma, rows, hidden, dtype, epsilon,
+                               weight_offset, *di);
+        p.scale_out = gs_out;
+        rmsq_status ls = launch(MODE_AMAX, p, residual != nullptr, dtype, *di, s);
+        if (ls != RMSQ_OK) return ls;
+    }
+    finalize_global_scale_kernel<<<1, 1, 0, s>>>(gs_out);
+    if (cudaGetLastError() != cudaSuccess) return RMSQ_ERR_LAUNCH;
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    return RMSQ_OK;
+}
+
+extern "C" const char* rmsq_status_string(rmsq_status status)
+{
+    switch (status) {
+    case RMSQ_OK: return "RMSQ_OK";
+    case RMSQ_ERR_NULL: return "RMSQ_ERR_NULL: a required pointer is NULL or residual pointers are unpaired";
+    case RMSQ_ERR_SHAPE: return "RMSQ_ERR_SHAPE: rows or hidden out of range, or hidden not a multiple of the block";
+    case RMSQ_ERR_ALIGN: return "RMSQ_ERR_ALIGN: a data pointer is not 16-byte aligned";
+    case RMSQ_ERR_DTYPE: return "RMSQ_ERR_DTYPE: unknown dtype, scale dtype or scale layout";
+    case RMSQ_ERR_LAUNCH: return "RMSQ_ERR_LAUNCH: the CUDA launch failed";
+    case RMSQ_ERR_VALUE: return "RMSQ_ERR_VALUE: epsilon, weight_offset or scale_ub out of range";
+    case RMSQ_ERR_DEVICE: return "RMSQ_ERR_DEVICE: no usable compute capability 10.3 device";
+    case RMSQ_ERR_TIMEOUT: return "RMSQ_ERR_TIMEOUT: a bounded device-side wait ran out";
+    }
+    return "RMSQ_UNKNOWN_STATUS";
+}
+
+extern "C" rmsq_status rmsq_device_status(void)
+{
+    const DeviceInfo* di = device_info();
+    if (!di) return RMSQ_ERR_DEVICE;
+    if (cudaDeviceSynchronize() != cudaSuccess) {
+        cudaGetLastError();
+        return RMSQ_ERR_LAUNCH;
+    }
+    unsigned int word = 0;
+    if (cudaMemcpyFromSymbol(&word, g_err_word, sizeof word) != cudaSuccess) {
+        cudaGetLastError();
+        return RMSQ_ERR_LAUNCH;
+    }
+    if (word != 0) {
+        const unsigned int zero = 0;
+        cudaMemcpyToSymbol(g_err_word, &zero, sizeof zero);
+        return RMSQ_ERR_TIMEOUT;
+    }
+    return RMSQ_OK;
+}
+
+extern "C" int rmsq_set_schedule(int schedule)
+{
+    if (schedule < 0 || schedule > 2) schedule = 0;
+    return g_schedule.exchange(schedule);
+}
+
+extern "C" rmsq_status rmsq_set_tuning(int stages, int ctas_per_sm, int vectors_per_thread)
+{
+    if (stages < 0 || stages > 8 || stages == 1 || ctas_per_sm < 0 || ctas_per_sm > 32 ||
+        (vectors_per_thread != 0 && vectors_per_thread != 1 && vectors_per_thread != 2 &&
+         vectors_per_thread != 4 && vectors_per_thread != 8))
+        return RMSQ_ERR_VALUE;
+    g_tune_stages = stages;
+    g_tune_ctas = ctas_per_sm;
+    g_tune_vpt = vectors_per_thread;
+    return RMSQ_OK;
+}
+
+extern "C" void rmsq_set_wait_timeout_ns(uint64_t timeout_ns)
+{
+    g_timeout_ns = timeout_ns > 0 ? timeout_ns : 1;
+}
+
+extern "C" rmsq_status rmsq_selftest_wait_timeout(uint64_t timeout_ns, void* stream)
+{
+    const DeviceInfo* di = device_info();
+    if (!di) return RMSQ_ERR_DEVICE;
+    if (timeout_ns > 10000000000ull) return RMSQ_ERR_VALUE;
+    selftest_wait_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(di->err, timeout_ns);
+    if (cudaGetLastError() != cudaSuccess) return RMSQ_ERR_LAUNCH;
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    return RMSQ_OK;
+}
+
+extern "C" rmsq_status rmsq_debug_convert(int fmt, const float* in, uint8_t* out, int64_t n,
+                                          void* stream)
+{
+    if (!in || !out) return RMSQ_ERR_NULL;
+    if (fmt != 0 && fmt != 1) return RMSQ_ERR_DTYPE;
+    if (n < 0) return RMSQ_ERR_SHAPE;
+    if (n == 0) return RMSQ_OK;
+    const DeviceInfo* di = device_info();
+    if (!di) return RMSQ_ERR_DEVICE;
+    long long blocks = (n + 255) / 256;
+    if (blocks > 8LL * di->sms * 8) blocks = 8LL * di->sms * 8;
+    debug_convert_kernel<<<static_cast<unsigned>(blocks), 256, 0, static_cast<cudaStream_t>(stream)>>>(
+        fmt, in, out, n);
+    if (cudaGetLastError() != cudaSuccess) return RMSQ_ERR_LAUNCH;
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    return RMSQ_OK;
+}
+
+extern "C" uint64_t rmsq_launch_count(void) { return g_launches.load(); }

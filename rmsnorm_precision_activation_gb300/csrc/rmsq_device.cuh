@@ -1,0 +1,873 @@
+// rmsq_device.cuh -- device code of the fused residual-add + RMSNorm + FP8 / NVFP4 / MXFP4 kernels
+// for sm_103a (GB300).
+//
+// One kernel template covers every mode, input type and schedule. A CTA owns whole rows: its T
+// threads split a row into 16-byte vectors (vector v of the row goes to thread v % T, so a warp
+// touches 512 contiguous bytes per step), add the residual, reduce the sum of squares over the
+// CTA, form y = s * rstd * (gamma + offset) and quantise. The row is read from HBM exactly once.
+//
+// Two schedules fetch the row:
+//   SCHED_PIPE  persistent CTAs with a ring of `stages` shared-memory row buffers filled by the
+//               TMA bulk-copy engine (cp.async.bulk + mbarrier transaction counts). Thread 0
+//               refills a buffer with the row `stages` iterations ahead as soon as the CTA has
+//               read it, so several rows per SM stay in flight while the CTA computes.
+//   SCHED_REG   persistent CTAs that load their row straight into registers with 128-bit
+//               streaming loads; latency is hidden by the other CTAs on the SM.
+//
+// Method sources: Modular Mojo API docs "rms_norm_fused_fp8" / "allreduce_residual_rmsnorm_fp8"
+// (FP8 row scale with scale_ub, residual_output, weight_offset on gamma) and FlashInfer
+// "cute_dsl/rmsnorm_fp4quant.py" (RMSNormFP4QuantKernel phases 2-3: rstd, block amax, E4M3 /
+// UE8M0 block scale, E2M1 packing, swizzled 128x4 scale layout).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace rmsq {
+
+enum { DT_BF16 = 0, DT_FP16 = 1, DT_F32 = 2 };
+// MODE_AMAX is the NVFP4 global-scale pre-pass: y is formed but only max |y| leaves the kernel.
+enum { MODE_FP8 = 0, MODE_NVFP4 = 1, MODE_MXFP4 = 2, MODE_AMAX = 3 };
+enum { SCHED_PIPE = 1, SCHED_REG = 2 };
+
+// Error flag bits set on the device.
+enum { ERRF_WAIT_TIMEOUT = 1u };
+
+struct Params {
+    const void* x;            // [rows x hidden]
+    const void* res;          // [rows x hidden] or null
+    void* res_out;            // [rows x hidden] or null
+    const void* gamma;        // [hidden]
+    void* out;                // codes
+    void* scale_out;          // FP8 row scales / FP4 block scales
+    const float* gs;          // NVFP4 global scale (device)
+    unsigned int* err;        // device error word
+    long long rows;
+    int nvec;                 // 16-byte vectors per row
+    int hidden;
+    float eps;
+    float offset;
+    float scale_ub;
+    int scale_dtype;          // FP8: DT_F32 / DT_BF16 / DT_FP16
+    int swizzled;             // FP4: swizzled 128x4 scale layout
+    int nsf;                  // FP4: block scales per row
+    int k_tiles;              // FP4 swizzled: 4-scale tiles per row
+    int stages;               // SCHED_PIPE: ring depth
+    unsigned long long timeout_ns;
+};
+
+// ------------------------------------------------------------------------------------------
+// PTX helpers (hand-written): mbarrier, bulk copy, timers, conversions
+// ------------------------------------------------------------------------------------------
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p)
+{
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init()
+{
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+// Orders this thread's earlier generic-proxy shared-memory accesses before later async-proxy
+// (bulk copy) accesses to the same buffer.
+__device__ __forceinline__ void fence_proxy_async_smem()
+{
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
+{
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+
+__device__ __forceinline__ unsigned long long globaltimer_ns()
+{
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Wait for the given phase of an mbarrier, for at most timeout_ns. Returns false on timeout.
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
+                                                  unsigned long long timeout_ns)
+{
+    if (mbar_try_wait(bar, parity)) return true;
+    const unsigned long long t0 = globaltimer_ns();
+    while (true) {
+#pragma unroll 1
+        for (int i = 0; i < 32; ++i)
+            if (mbar_try_wait(bar, parity)) return true;
+        if (globaltimer_ns() - t0 > timeout_ns) return false;
+    }
+}
+
+__device__ __forceinline__ uint64_t l2_evict_first_policy()
+{
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
+// Global -> shared bulk copy (TMA engine), completion counted on `bar` in bytes.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes,
+                                          uint32_t bar, uint64_t policy)
+{
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1], %2, [%3], %4;" ::"r"(dst),
+        "l"(src), "r"(bytes), "r"(bar), "l"(policy)
+        : "memory");
+}
+
+__device__ __forceinline__ uint4 ld_stream_v4(const uint4* p)
+{
+    uint4 v;
+    asm volatile("ld.global.cs.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr)
+{
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(addr));
+    return v;
+}
+
+__device__ __forceinline__ void st_v4(void* p, uint4 v)
+{
+    asm volatile("st.global.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z),
+                 "r"(v.w)
+                 : "memory");
+}
+
+__device__ __forceinline__ void st_v2(void* p, uint32_t a, uint32_t b)
+{
+    asm volatile("st.global.v2.u32 [%0], {%1, %2};" ::"l"(p), "r"(a), "r"(b) : "memory");
+}
+
+__device__ __forceinline__ void st_u32(void* p, uint32_t a)
+{
+    asm volatile("st.global.u32 [%0], %1;" ::"l"(p), "r"(a) : "memory");
+}
+
+__device__ __forceinline__ void st_u16(void* p, uint16_t a)
+{
+    asm volatile("st.global.u16 [%0], %1;" ::"l"(p), "h"(a) : "memory");
+}
+
+// Two fp32 -> two E4M3 codes (round to nearest even, satfinite); `lo` lands in the low byte.
+__device__ __forceinline__ uint32_t cvt_e4m3x2(float lo, float hi)
+{
+    uint16_t r;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+// Eight fp32 -> eight E2M1 codes packed in a u32 (RNE, satfinite); element j in nibble j.
+__device__ __forceinline__ uint32_t cvt_e2m1x8(const float (&v)[8])
+{
+    uint32_t r;
+    asm("{\n\t.reg .b8 q0, q1, q2, q3;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 q0, %2, %1;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 q1, %4, %3;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 q2, %6, %5;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 q3, %8, %7;\n\t"
+        "mov.b32 %0, {q0, q1, q2, q3};\n\t}"
+        : "=r"(r)
+        : "f"(v[0]), "f"(v[1]), "f"(v[2]), "f"(v[3]), "f"(v[4]), "f"(v[5]), "f"(v[6]), "f"(v[7]));
+    return r;
+}
+
+// Four fp32 -> four E2M1 codes in the low 16 bits.
+__device__ __forceinline__ uint32_t cvt_e2m1x4(const float (&v)[4])
+{
+    uint32_t r;
+    asm("{\n\t.reg .b8 q0, q1;\n\t.reg .b16 h;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 q0, %2, %1;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 q1, %4, %3;\n\t"
+        "mov.b16 h, {q0, q1};\n\t"
+        "cvt.u32.u16 %0, h;\n\t}"
+        : "=r"(r)
+        : "f"(v[0]), "f"(v[1]), "f"(v[2]), "f"(v[3]));
+    return r;
+}
+
+// Exact value of an E4M3 code (hardware e4m3 -> f16 conversion is exact, subnormals included).
+__device__ __forceinline__ float e4m3_value(uint32_t code)
+{
+    uint32_t h2;
+    const uint16_t c = static_cast<uint16_t>(code & 0xFFu);
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(c));
+    float f;
+    asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %1;\n\tcvt.f32.f16 %0, l;\n\t}" : "=f"(f) : "r"(h2));
+    return f;
+}
+
+// ------------------------------------------------------------------------------------------
+// Element types: 16-byte vectors of bf16 / fp16 (8 elements) or fp32 (4 elements)
+// ------------------------------------------------------------------------------------------
+
+template <int DT> struct Elem;
+
+template <> struct Elem<DT_BF16> {
+    static constexpr int EPV = 8;
+    // Element pairs (2j, 2j+1) as float2, exact.
+    static __device__ __forceinline__ void pairs(const uint4& v, float2 (&f)[4])
+    {
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            f[i] = make_float2(__uint_as_float(w[i] << 16), __uint_as_float(w[i] & 0xFFFF0000u));
+    }
+    static __device__ __forceinline__ void unpack(const uint4& v, float (&f)[8])
+    {
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            f[2 * i] = __uint_as_float(w[i] << 16);
+            f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+        }
+    }
+    // Correctly rounded bf16 sums (add.rn.bf16x2).
+    static __device__ __forceinline__ uint4 add(const uint4& a, const uint4& b)
+    {
+        uint4 r;
+        asm("add.rn.bf16x2 %0, %1, %2;" : "=r"(r.x) : "r"(a.x), "r"(b.x));
+        asm("add.rn.bf16x2 %0, %1, %2;" : "=r"(r.y) : "r"(a.y), "r"(b.y));
+        asm("add.rn.bf16x2 %0, %1, %2;" : "=r"(r.z) : "r"(a.z), "r"(b.z));
+        asm("add.rn.bf16x2 %0, %1, %2;" : "=r"(r.w) : "r"(a.w), "r"(b.w));
+        return r;
+    }
+};
+
+template <> struct Elem<DT_FP16> {
+    static constexpr int EPV = 8;
+    static __device__ __forceinline__ void pairs(const uint4& v, float2 (&f)[4])
+    {
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            float lo, hi;
+            asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\t"
+                "cvt.f32.f16 %0, l;\n\tcvt.f32.f16 %1, h;\n\t}"
+                : "=f"(lo), "=f"(hi)
+                : "r"(w[i]));
+            f[i] = make_float2(lo, hi);
+        }
+    }
+    static __device__ __forceinline__ void unpack(const uint4& v, float (&f)[8])
+    {
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            float lo, hi;
+            asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\t"
+                "cvt.f32.f16 %0, l;\n\tcvt.f32.f16 %1, h;\n\t}"
+                : "=f"(lo), "=f"(hi)
+                : "r"(w[i]));
+            f[2 * i] = lo;
+            f[2 * i + 1] = hi;
+        }
+    }
+    static __device__ __forceinline__ uint4 add(const uint4& a, const uint4& b)
+    {
+        uint4 r;
+        asm("add.rn.f16x2 %0, %1, %2;" : "=r"(r.x) : "r"(a.x), "r"(b.x));
+        asm("add.rn.f16x2 %0, %1, %2;" : "=r"(r.y) : "r"(a.y), "r"(b.y));
+        asm("add.rn.f16x2 %0, %1, %2;" : "=r"(r.z) : "r"(a.z), "r"(b.z));
+        asm("add.rn.f16x2 %0, %1, %2;" : "=r"(r.w) : "r"(a.w), "r"(b.w));
+        return r;
+    }
+};
+
+template <> struct Elem<DT_F32> {
+    static constexpr int EPV = 4;
+    static __device__ __forceinline__ void pairs(const uint4& v, float2 (&f)[2])
+    {
+        f[0] = make_float2(__uint_as_float(v.x), __uint_as_float(v.y));
+        f[1] = make_float2(__uint_as_float(v.z), __uint_as_float(v.w));
+    }
+    static __device__ __forceinline__ void unpack(const uint4& v, float (&f)[4])
+    {
+        f[0] = __uint_as_float(v.x);
+        f[1] = __uint_as_float(v.y);
+        f[2] = __uint_as_float(v.z);
+        f[3] = __uint_as_float(v.w);
+    }
+    static __device__ __forceinline__ uint4 add(const uint4& a, const uint4& b)
+    {
+        uint4 r;
+        r.x = __float_as_uint(__fadd_rn(__uint_as_float(a.x), __uint_as_float(b.x)));
+        r.y = __float_as_uint(__fadd_rn(__uint_as_float(a.y), __uint_as_float(b.y)));
+        r.z = __float_as_uint(__fadd_rn(__uint_as_float(a.z), __uint_as_float(b.z)));
+        r.w = __float_as_uint(__fadd_rn(__uint_as_float(a.w), __uint_as_float(b.w)));
+        return r;
+    }
+};
+
+// Packed fp32 pairs (Blackwell f32x2 instructions: two IEEE round-to-nearest operations per
+// instruction).
+__device__ __forceinline__ float2 add2(float2 a, float2 b)
+{
+    float2 r;
+    asm("{\n\t.reg .b64 pa, pb, pd;\n\tmov.b64 pa, {%2, %3};\n\tmov.b64 pb, {%4, %5};\n\t"
+        "add.rn.f32x2 pd, pa, pb;\n\tmov.b64 {%0, %1}, pd;\n\t}"
+        : "=f"(r.x), "=f"(r.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return r;
+}
+
+__device__ __forceinline__ float2 sub2(float2 a, float2 b)
+{
+    float2 r;
+    asm("{\n\t.reg .b64 pa, pb, pd;\n\tmov.b64 pa, {%2, %3};\n\tmov.b64 pb, {%4, %5};\n\t"
+        "sub.rn.f32x2 pd, pa, pb;\n\tmov.b64 {%0, %1}, pd;\n\t}"
+        : "=f"(r.x), "=f"(r.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return r;
+}
+
+__device__ __forceinline__ float2 mul2(float2 a, float2 b)
+{
+    float2 r;
+    asm("{\n\t.reg .b64 pa, pb, pd;\n\tmov.b64 pa, {%2, %3};\n\tmov.b64 pb, {%4, %5};\n\t"
+        "mul.rn.f32x2 pd, pa, pb;\n\tmov.b64 {%0, %1}, pd;\n\t}"
+        : "=f"(r.x), "=f"(r.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return r;
+}
+
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c)
+{
+    float2 r;
+    asm("{\n\t.reg .b64 pa, pb, pc, pd;\n\tmov.b64 pa, {%2, %3};\n\tmov.b64 pb, {%4, %5};\n\t"
+        "mov.b64 pc, {%6, %7};\n\tfma.rn.f32x2 pd, pa, pb, pc;\n\tmov.b64 {%0, %1}, pd;\n\t}"
+        : "=f"(r.x), "=f"(r.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+    return r;
+}
+
+__device__ __forceinline__ float max3(float a, float b, float c)
+{
+    float r;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
+
+__device__ __forceinline__ float2 splat(float v) { return make_float2(v, v); }
+
+__device__ __forceinline__ float warp_sum(float v)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+    return v;
+}
+
+__device__ __forceinline__ float warp_max(float v)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
+    return v;
+}
+
+// UE8M0 code of a block with max |y| = a >= 0: the smallest e with 6 * 2^e >= a, plus 127,
+// clamped to [0, 255]; 0 for a = 0. Exact, from a's bits: for a = m * 2^E with m in [1, 2),
+// a / 6 <= 2^(E-2) exactly when m <= 1.5, so e = E - 2 if m <= 1.5 and E - 1 otherwise.
+// Subnormal a (< 2^-126) gives e <= -128, hence code 0.
+__device__ __forceinline__ uint32_t ue8m0_code(float a)
+{
+    const uint32_t bits = __float_as_uint(a);
+    const int biased = static_cast<int>(bits >> 23);          // a >= 0: no sign bit
+    if (biased == 0) return 0u;                                // zero or subnormal
+    const int e = biased - 127 - 2 + ((bits & 0x7FFFFFu) > 0x400000u ? 1 : 0);
+    int code = e + 127;
+    code = code < 0 ? 0 : (code > 255 ? 255 : code);
+    return static_cast<uint32_t>(code);
+}
+
+// 2^(127 - code) for code in [1, 254] (exact), 0 for code 0.
+__device__ __forceinline__ float ue8m0_inv_factor(uint32_t code)
+{
+    return code == 0u ? 0.0f : __uint_as_float((254u - code) << 23);
+}
+
+__device__ __forceinline__ long long scale_offset(long long row, int sf, int nsf, int swizzled,
+                                                  int k_tiles)
+{
+    if (!swizzled) return row * nsf + sf;
+    return (row >> 7) * (static_cast<long long>(k_tiles) * 512) + (sf >> 2) * 512 +
+           (row & 31) * 16 + ((row & 127) >> 5) * 4 + (sf & 3);
+}
+
+// ------------------------------------------------------------------------------------------
+// Exactly rounded row math (FP8)
+//
+// FP8 codes are decided by comparing y / scale with rounding boundaries. With 16-bit inputs,
+// y_i / scale = 448 * (s_i w_i) / (s_m w_m) in exact arithmetic (rstd cancels): a ratio of short
+// numbers that lands on a boundary far more often than random data would, so the way such a
+// near-tie goes is decided by the fp32 roundings of rstd, y and the scale. The FP8 kernel
+// therefore forms rstd, y and the scale as the correctly rounded fp32 values of their definitions
+// and rounds the exact quotient y / scale to E4M3:
+//   sum of squares  compensated (TwoSum) fp32 accumulation: hi + lo within ~2^-45 of the exact sum
+//   rstd            RN(1 / sqrt(sum / H + eps)) from one Newton step in float-float arithmetic
+//   y               RN(s * w * rstd) with s * w split exactly by an FMA
+//   y / scale       rounded to odd in fp32 (RN quotient, exact remainder, then RZ with a sticky
+//                   last bit), so that the E4M3 RNE conversion rounds the exact quotient
+// FP4 codes see no such cancellation (the block scale is itself rounded, or a power of two applied
+// to y exactly), so the FP4 kernels and the amax pre-pass use a plain fp32 sum of squares and the
+// correctly rounded rsqrt of the rounded mean.
+// ------------------------------------------------------------------------------------------
+
+struct FF {
+    float hi, lo;
+};
+
+// a + b = s.hi + s.lo exactly (TwoSum; no ordering assumption).
+__device__ __forceinline__ FF two_sum(float a, float b)
+{
+    const float s = __fadd_rn(a, b);
+    const float bb = __fsub_rn(s, a);
+    const float e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb));
+    return FF{s, e};
+}
+
+__device__ __forceinline__ FF ff_add(FF a, FF b)
+{
+    FF s = two_sum(a.hi, b.hi);
+    s.lo = __fadd_rn(s.lo, __fadd_rn(a.lo, b.lo));
+    return s;
+}
+
+// TwoSum on two independent lanes.
+__device__ __forceinline__ void two_sum2(float2 a, float2 b, float2& s, float2& e)
+{
+    s = add2(a, b);
+    const float2 bb = sub2(s, a);
+    e = add2(sub2(a, sub2(s, bb)), sub2(b, bb));
+}
+
+__device__ __forceinline__ FF shfl_xor_ff(FF v, int o)
+{
+    return FF{__shfl_xor_sync(0xFFFFFFFFu, v.hi, o), __shfl_xor_sync(0xFFFFFFFFu, v.lo, o)};
+}
+
+// RN_fp32(1 / sqrt(ss / H + eps)) for ss = hi + lo.
+__device__ __forceinline__ float rstd_from_sum(FF ss, float H, float eps)
+{
+    const float q = __fdiv_rn(ss.hi, H);
+    const float rem = fmaf(-q, H, ss.hi);                     // exact remainder of the division
+    const float q_lo = __fdiv_rn(__fadd_rn(rem, ss.lo), H);
+    FF m = two_sum(q, eps);
+    m.lo = __fadd_rn(m.lo, q_lo);
+    if (!(m.hi > 0.0f)) return __int_as_float(0x7F800000);    // 1 / sqrt(0)
+    const float r0 = rsqrtf(m.hi);
+    const float p_hi = __fmul_rn(r0, r0);
+    const float p_lo = fmaf(r0, r0, -p_hi);
+    const float t_hi = __fmul_rn(m.hi, p_hi);
+    const float t_lo = __fadd_rn(fmaf(m.hi, p_hi, -t_hi), fmaf(m.hi, p_lo, __fmul_rn(m.lo, p_hi)));
+    const float e = __fsub_rn(__fsub_rn(1.0f, t_hi), t_lo);   // 1 - m r0^2, t_hi ~ 1 so exact
+    return __fadd_rn(r0, __fmul_rn(__fmul_rn(r0, 0.5f), e));
+}
+
+// RN(s * w * rstd) on a pair: s * w = hi + lo exactly, then one rounding of hi rstd + lo rstd.
+__device__ __forceinline__ float2 norm_mul2(float2 s, float2 w, float2 rstd)
+{
+    const float2 hi = mul2(s, w);
+    const float2 lo = fma2(s, w, make_float2(-hi.x, -hi.y));
+    return fma2(hi, rstd, mul2(lo, rstd));
+}
+
+// Round-to-odd fp32 quotient y / d on a pair (d > 0), from inv = RN(1 / d) and nd = -d:
+// q = RN(y / d) by one correction step, r = y - q d exactly; then q moves one unit toward zero
+// when |y / d| < |q| and gets its last bit set whenever the division was inexact. The result
+// is RZ(y / d) with a sticky bit, so a later rounding to a format with at least two fewer bits
+// equals the correctly rounded exact quotient.
+__device__ __forceinline__ float ro_bits(float q, float r)
+{
+    const uint32_t b = __float_as_uint(q);
+    const uint32_t rb = __float_as_uint(r);
+    const bool inexact = ((rb << 1) != 0u) && ((b << 1) != 0u);
+    const uint32_t toward_zero = (rb ^ b) >> 31;
+    return __uint_as_float(inexact ? ((b - toward_zero) | 1u) : b);
+}
+
+__device__ __forceinline__ float2 div_odd2(float2 y, float2 nd, float2 inv)
+{
+    const float2 q0 = mul2(y, inv);
+    const float2 q = fma2(fma2(q0, nd, y), inv, q0);
+    const float2 r = fma2(q, nd, y);
+    return make_float2(ro_bits(q.x, r.x), ro_bits(q.y, r.y));
+}
+
+// Shared memory after the stage ring: [2][32] float2 sum-of-squares partials, [32] row amax,
+// [128] NVFP4 element factors gs / dec(s) indexed by the E4M3 block-scale code.
+constexpr int kRedFloats = 2 * 32 * 2 + 32 + 128;
+
+// ------------------------------------------------------------------------------------------
+// The kernel
+// ------------------------------------------------------------------------------------------
+
+template <int DT, bool RES, int MODE, int VPT, int SCHED>
+__global__ void __launch_bounds__(512, 1)
+rmsq_row_kernel(const Params p)
+{
+    using E = Elem<DT>;
+    constexpr int EPV = E::EPV;
+    constexpr int NP = EPV / 2;                                      // element pairs per vector
+    constexpr int BLOCK = MODE == MODE_NVFP4 ? 16 : 32;             // FP4 scale block
+    constexpr int GROUP = MODE == MODE_FP8 ? 1 : BLOCK / EPV;        // lanes per FP4 block
+    constexpr bool EXACT = MODE == MODE_FP8;
+    constexpr bool KEEP_Y = VPT <= 4;                                // FP8: y held in registers
+
+    extern __shared__ __align__(128) unsigned char smem[];
+
+    const int tid = threadIdx.x;
+    const int T = blockDim.x;
+    const int lane = tid & 31;
+    const int warp = tid >> 5;
+    const int nwarps = T >> 5;
+    const int nv = p.nvec;
+    const uint32_t row_bytes = static_cast<uint32_t>(nv) * 16u;
+    const uint32_t stage_bytes = row_bytes * (RES ? 2u : 1u);
+    const int S = SCHED == SCHED_PIPE ? p.stages : 0;
+
+    float* red = reinterpret_cast<float*>(smem + static_cast<size_t>(S) * stage_bytes);
+    float2* red_ss_all = reinterpret_cast<float2*>(red);                    // [2][32]
+    float* red_max = red + 128;                                             // [32]
+    float* nv_factor = red + 160;                                           // [128]
+    uint64_t* bars = reinterpret_cast<uint64_t*>(red + kRedFloats);         // [S]
+
+    const uint4* __restrict__ xg = static_cast<const uint4*>(p.x);
+    const uint4* __restrict__ rg = static_cast<const uint4*>(p.res);
+    uint4* __restrict__ rog = static_cast<uint4*>(p.res_out);
+
+    float gs = 1.0f, gs_over_6 = 0.0f;
+    if constexpr (MODE == MODE_NVFP4) {
+        gs = __ldg(p.gs);
+        gs_over_6 = __fdiv_rn(gs, 6.0f);
+        // factor[c] = gs / dec(c) for every positive E4M3 code (0 for code 0 and for NaN)
+        for (int c = tid; c < 128; c += T) {
+            const float ds = e4m3_value(static_cast<uint32_t>(c));
+            nv_factor[c] = (c == 0 || c == 0x7F) ? 0.0f : __fdiv_rn(gs, ds);
+        }
+    }
+
+    uint64_t policy = 0;
+    if constexpr (SCHED == SCHED_PIPE) {
+        policy = l2_evict_first_policy();
+        if (tid == 0) {
+            for (int s = 0; s < S; ++s) mbar_init(smem_u32(&bars[s]), 1);
+            fence_mbar_init();
+        }
+        __syncthreads();
+        if (tid == 0) {
+            for (int s = 0; s < S; ++s) {
+                const long long row = blockIdx.x + static_cast<long long>(s) * gridDim.x;
+                if (row >= p.rows) break;
+                const uint32_t bar = smem_u32(&bars[s]);
+                const uint32_t dst = smem_u32(smem + static_cast<size_t>(s) * stage_bytes);
+                mbar_arrive_expect_tx(bar, stage_bytes);
+                bulk_load(dst, xg + row * nv, row_bytes, bar, policy);
+                if constexpr (RES) bulk_load(dst + row_bytes, rg + row * nv, row_bytes, bar, policy);
+            }
+        }
+    } else if constexpr (MODE == MODE_NVFP4) {
+        __syncthreads();
+    }
+
+    // gamma stays packed in registers for the CTA's lifetime; the offset is added per use in
+    // fp32 (w = fp32(gamma) + fp32(weight_offset)).
+    uint4 g[VPT];
+#pragma unroll
+    for (int k = 0; k < VPT; ++k) {
+        const int v = tid + k * T;
+        g[k] = v < nv ? __ldg(static_cast<const uint4*>(p.gamma) + v) : make_uint4(0, 0, 0, 0);
+    }
+    const float2 offset2 = splat(p.offset);
+    const float Hf = static_cast<float>(p.hidden);
+    // lanes in the second reduction stage: the smallest power of two >= nwarps
+    int red_lanes = 1;
+    while (red_lanes < nwarps) red_lanes <<= 1;
+
+    float run_max = 0.0f;   // MODE_AMAX: max |y| over this thread's share of the CTA's rows
+    long long it = 0;
+    for (long long row = blockIdx.x; row < p.rows; row += gridDim.x, ++it) {
+        // ---- load the row, add the residual, write residual_output, sum of squares ----------
+        bool timed_out = false;
+        uint32_t stage_addr = 0;
+        int stage = 0;
+        if constexpr (SCHED == SCHED_PIPE) {
+            stage = static_cast<int>(it % S);
+            const uint32_t parity = static_cast<uint32_t>((it / S) & 1);
+            stage_addr = smem_u32(smem + static_cast<size_t>(stage) * stage_bytes);
+            timed_out = !mbar_wait_bounded(smem_u32(&bars[stage]), parity, p.timeout_ns);
+        }
+        uint4 s[VPT];
+        float2 acc_hi = make_float2(0.0f, 0.0f), acc_lo = make_float2(0.0f, 0.0f);
+#pragma unroll
+        for (int k = 0; k < VPT; ++k) {
+            const int v = tid + k * T;
+            s[k] = make_uint4(0, 0, 0, 0);
+            if (v < nv && !timed_out) {
+                uint4 xv, rv;
+                if constexpr (SCHED == SCHED_PIPE) {
+                    xv = ld_shared_v4(stage_addr + v * 16u);
+                    if constexpr (RES) rv = ld_shared_v4(stage_addr + row_bytes + v * 16u);
+                } else {
+                    xv = ld_stream_v4(xg + row * nv + v);
+                    if constexpr (RES) rv = ld_stream_v4(rg + row * nv + v);
+                }
+                if constexpr (RES) {
+                    s[k] = E::add(xv, rv);
+                    if constexpr (MODE != MODE_AMAX) st_v4(rog + row * nv + v, s[k]);
+                } else {
+                    s[k] = xv;
+                }
+                float2 f[NP];
+                E::pairs(s[k], f);
+#pragma unroll
+                for (int j = 0; j < NP; ++j) {
+                    if constexpr (EXACT) {
+                        const float2 sq = mul2(f[j], f[j]);          // exact for 16-bit inputs
+                        float2 t, e;
+                        two_sum2(acc_hi, sq, t, e);
+                        acc_hi = t;
+                        acc_lo = add2(acc_lo, e);
+                        if constexpr (DT == DT_F32)
+                            acc_lo = add2(acc_lo, fma2(f[j], f[j], make_float2(-sq.x, -sq.y)));
+                    } else {
+                        acc_hi = fma2(f[j], f[j], acc_hi);
+                    }
+                }
+            }
+        }
+        // ---- CTA reduction of the sum of squares -> rstd ----------------------------------
+        float2* red_ss = red_ss_all + (it & 1) * 32;
+        FF ss;
+        if constexpr (EXACT) {
+            ss = ff_add(FF{acc_hi.x, acc_lo.x}, FF{acc_hi.y, acc_lo.y});
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) ss = ff_add(ss, shfl_xor_ff(ss, o));
+        } else {
+            ss = FF{warp_sum(__fadd_rn(acc_hi.x, acc_hi.y)), 0.0f};
+        }
+        if (lane == 0) red_ss[warp] = make_float2(ss.hi, ss.lo);
+        if (__syncthreads_or(timed_out)) {
+            if constexpr (SCHED == SCHED_PIPE) {
+                if (tid == 0) {
+                    atomicOr(p.err, ERRF_WAIT_TIMEOUT);
+                    // let the copies already issued for later rows land (bounded) before exit
+                    for (int j = 1; j < S; ++j) {
+                        const long long jrow = row + static_cast<long long>(j) * gridDim.x;
+                        if (jrow >= p.rows) break;
+                        const long long jit = it + j;
+                        mbar_wait_bounded(smem_u32(&bars[jit % S]),
+                                          static_cast<uint32_t>((jit / S) & 1), p.timeout_ns);
+                    }
+                }
+            }
+            return;
+        }
+        if constexpr (SCHED == SCHED_PIPE) {
+            // Every thread has read this buffer: refill it with the row S iterations ahead.
+            const long long nrow = row + static_cast<long long>(S) * gridDim.x;
+            if (tid == 0 && nrow < p.rows) {
+                fence_proxy_async_smem();
+                const uint32_t bar = smem_u32(&bars[stage]);
+                mbar_arrive_expect_tx(bar, stage_bytes);
+                bulk_load(stage_addr, xg + nrow * nv, row_bytes, bar, policy);
+                if constexpr (RES)
+                    bulk_load(stage_addr + row_bytes, rg + nrow * nv, row_bytes, bar, policy);
+            }
+        }
+        float rstd;
+        {
+            const float2 part = lane < nwarps ? red_ss[lane] : make_float2(0.0f, 0.0f);
+            if constexpr (EXACT) {
+                FF t{part.x, part.y};
+                for (int o = red_lanes >> 1; o > 0; o >>= 1) t = ff_add(t, shfl_xor_ff(t, o));
+                t.hi = __shfl_sync(0xFFFFFFFFu, t.hi, 0);
+                t.lo = __shfl_sync(0xFFFFFFFFu, t.lo, 0);
+                rstd = rstd_from_sum(t, Hf, p.eps);
+            } else {
+                float t = part.x;
+                for (int o = red_lanes >> 1; o > 0; o >>= 1) t += __shfl_xor_sync(0xFFFFFFFFu, t, o);
+                t = __shfl_sync(0xFFFFFFFFu, t, 0);
+                rstd = __frsqrt_rn(__fadd_rn(__fdiv_rn(t, Hf), p.eps));
+            }
+        }
+        const float2 rstd2 = splat(rstd);
+
+        if constexpr (MODE == MODE_AMAX) {
+#pragma unroll
+            for (int k = 0; k < VPT; ++k) {
+                float2 f[NP], gw[NP];
+                E::pairs(s[k], f);
+                E::pairs(g[k], gw);
+#pragma unroll
+                for (int j = 0; j < NP; ++j) {
+                    const float2 y = mul2(mul2(f[j], add2(gw[j], offset2)), rstd2);
+                    run_max = max3(run_max, fabsf(y.x), fabsf(y.y));
+                }
+            }
+        } else if constexpr (MODE == MODE_FP8) {
+            // ---- y, row amax, scale, E4M3 codes ----------------------------------------------
+            float2 y[KEEP_Y ? VPT : 1][NP];
+            float amax = 0.0f;
+#pragma unroll
+            for (int k = 0; k < VPT; ++k) {
+                float2 f[NP], gw[NP];
+                E::pairs(s[k], f);
+                E::pairs(g[k], gw);
+#pragma unroll
+                for (int j = 0; j < NP; ++j) {
+                    const float2 yy = norm_mul2(f[j], add2(gw[j], offset2), rstd2);
+                    if constexpr (KEEP_Y) y[k][j] = yy;
+                    amax = max3(amax, fabsf(yy.x), fabsf(yy.y));
+                }
+            }
+            amax = warp_max(amax);
+            if (lane == 0) red_max[warp] = amax;
+            __syncthreads();
+            amax = lane < nwarps ? red_max[lane] : 0.0f;
+            for (int o = red_lanes >> 1; o > 0; o >>= 1)
+                amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
+            amax = __shfl_sync(0xFFFFFFFFu, amax, 0);
+            float scale = __fdiv_rn(fminf(amax, p.scale_ub), 448.0f);
+            if (p.scale_dtype == DT_BF16) {
+                uint16_t h;
+                asm("cvt.rn.bf16.f32 %0, %1;" : "=h"(h) : "f"(scale));
+                scale = __uint_as_float(static_cast<uint32_t>(h) << 16);
+                if (tid == 0) static_cast<uint16_t*>(p.scale_out)[row] = h;
+            } else if (p.scale_dtype == DT_FP16) {
+                uint16_t h;
+                asm("cvt.rn.f16.f32 %0, %1;" : "=h"(h) : "f"(scale));
+                asm("cvt.f32.f16 %0, %1;" : "=f"(scale) : "h"(h));
+                if (tid == 0) static_cast<uint16_t*>(p.scale_out)[row] = h;
+            } else {
+                if (tid == 0) static_cast<float*>(p.scale_out)[row] = scale;
+            }
+            const bool zero_row = !(scale > 0.0f);
+            const float2 inv2 = splat(zero_row ? 0.0f : __frcp_rn(scale));
+            const float2 nd2 = splat(-scale);
+            unsigned char* outp = static_cast<unsigned char*>(p.out) + row * p.hidden;
+#pragma unroll
+            for (int k = 0; k < VPT; ++k) {
+                const int v = tid + k * T;
+                if (v >= nv) continue;
+                float2 yk[NP];
+                if constexpr (KEEP_Y) {
+#pragma unroll
+                    for (int j = 0; j < NP; ++j) yk[j] = y[k][j];
+                } else {
+                    float2 f[NP], gw[NP];
+                    E::pairs(s[k], f);
+                    E::pairs(g[k], gw);
+#pragma unroll
+                    for (int j = 0; j < NP; ++j) yk[j] = norm_mul2(f[j], add2(gw[j], offset2), rstd2);
+                }
+                uint32_t c[NP];
+#pragma unroll
+                for (int j = 0; j < NP; ++j) {
+                    const float2 q = div_odd2(yk[j], nd2, inv2);
+                    c[j] = zero_row ? 0u : cvt_e4m3x2(q.x, q.y);
+                }
+                if constexpr (EPV == 8) {
+                    st_v2(outp + v * 8, c[0] | (c[1] << 16), c[2] | (c[3] << 16));
+                } else {
+                    st_u32(outp + v * 4, c[0] | (c[1] << 16));
+                }
+            }
+        } else {
+            // ---- FP4: per-block amax across GROUP adjacent lanes, scale, E2M1 ---------------
+            unsigned char* outp = static_cast<unsigned char*>(p.out) + row * (p.hidden / 2);
+            unsigned char* sp = static_cast<unsigned char*>(p.scale_out);
+#pragma unroll
+            for (int k = 0; k < VPT; ++k) {
+                const int v = tid + k * T;
+                float2 y[NP];
+                float m = 0.0f;
+                {
+                    float2 f[NP], gw[NP];
+                    E::pairs(s[k], f);
+                    E::pairs(g[k], gw);
+#pragma unroll
+                    for (int j = 0; j < NP; ++j) {
+                        y[j] = mul2(mul2(f[j], add2(gw[j], offset2)), rstd2);
+                        m = max3(m, fabsf(y[j].x), fabsf(y[j].y));
+                    }
+                }
+#pragma unroll
+                for (int o = 1; o < GROUP; o <<= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+                float factor;
+                uint32_t code;
+                if constexpr (MODE == MODE_NVFP4) {
+                    const float t = fminf(__fmul_rn(m, gs_over_6), 448.0f);
+                    code = cvt_e4m3x2(t, 0.0f) & 0xFFu;
+                    factor = nv_factor[code & 0x7Fu];
+                } else {
+                    code = ue8m0_code(m);
+                    factor = ue8m0_inv_factor(code);
+                }
+                if (v >= nv) continue;
+                if ((v & (GROUP - 1)) == 0)
+                    sp[scale_offset(row, v / GROUP, p.nsf, p.swizzled, p.k_tiles)] =
+                        static_cast<unsigned char>(code);
+                const bool zero_block = !(factor > 0.0f);
+                const float2 f2 = splat(factor);
+                if constexpr (EPV == 8) {
+                    float q[8];
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const float2 qq = mul2(y[j], f2);
+                        q[2 * j] = qq.x;
+                        q[2 * j + 1] = qq.y;
+                    }
+                    st_u32(outp + v * 4, zero_block ? 0u : cvt_e2m1x8(q));
+                } else {
+                    float q[4];
+#pragma unroll
+                    for (int j = 0; j < 2; ++j) {
+                        const float2 qq = mul2(y[j], f2);
+                        q[2 * j] = qq.x;
+                        q[2 * j + 1] = qq.y;
+                    }
+                    st_u16(outp + v * 2, static_cast<uint16_t>(zero_block ? 0u : cvt_e2m1x4(q)));
+                }
+            }
+        }
+    }
+    if constexpr (MODE == MODE_AMAX) {
+        // non-negative floats order like their bit patterns, so an unsigned max is a float max
+        run_max = warp_max(run_max);
+        if (lane == 0 && run_max > 0.0f)
+            atomicMax(static_cast<unsigned int*>(p.scale_out), __float_as_uint(run_max));
+    }
+}
+
+}  // namespace rmsq

@@ -1,0 +1,72 @@
+// rmsq_host.h -- host-side plumbing shared by the library's translation units: the launch plan
+// and the per-mode dispatch entry points (each mode's kernels live in their own .cu file so the
+// build compiles them in parallel).
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include "rmsq_device.cuh"
+
+namespace rmsq {
+
+struct Plan {
+    int mode;          // MODE_*
+    int dt;            // DT_*
+    bool res;          // residual present
+    int vpt;           // 16-byte vectors per thread per row: 1, 2, 4 or 8
+    int sched;         // SCHED_PIPE or SCHED_REG
+    int threads;       // CTA size (multiple of 32)
+    int stages;        // SCHED_PIPE ring depth
+    int smem;          // dynamic shared memory bytes
+    int ctas_per_sm;   // cap on resident CTAs per SM (0: occupancy limit)
+};
+
+// Launch `fn` (a rmsq_row_kernel instantiation) with the plan: sets the dynamic shared memory
+// limit once per function and device, sizes a persistent grid of min(rows, CTAs per SM x SMs).
+cudaError_t run_kernel(const void* fn, const Plan& plan, const Params& p, cudaStream_t stream);
+
+// Per-mode dispatch on (dtype, residual, vpt, schedule); defined in rmsq_<mode>.cu.
+cudaError_t dispatch_fp8(const Plan& plan, const Params& p, cudaStream_t stream);
+cudaError_t dispatch_nvfp4(const Plan& plan, const Params& p, cudaStream_t stream);
+cudaError_t dispatch_mxfp4(const Plan& plan, const Params& p, cudaStream_t stream);
+cudaError_t dispatch_amax(const Plan& plan, const Params& p, cudaStream_t stream);
+
+// Instantiates the dispatch switch for one mode inside a .cu file.
+#define RMSQ_DEFINE_DISPATCH(NAME, MODE)                                                         \
+    template <int DT, bool RES, int VPT, int SCHED>                                               \
+    static cudaError_t NAME##_go(const Plan& pl, const Params& p, cudaStream_t st)                \
+    {                                                                                             \
+        return run_kernel(reinterpret_cast<const void*>(&rmsq_row_kernel<DT, RES, MODE, VPT, SCHED>), \
+                          pl, p, st);                                                             \
+    }                                                                                             \
+    template <int DT, bool RES, int VPT>                                                          \
+    static cudaError_t NAME##_sched(const Plan& pl, const Params& p, cudaStream_t st)             \
+    {                                                                                             \
+        return pl.sched == SCHED_PIPE ? NAME##_go<DT, RES, VPT, SCHED_PIPE>(pl, p, st)            \
+                                      : NAME##_go<DT, RES, VPT, SCHED_REG>(pl, p, st);            \
+    }                                                                                             \
+    template <int DT, bool RES>                                                                   \
+    static cudaError_t NAME##_vpt(const Plan& pl, const Params& p, cudaStream_t st)               \
+    {                                                                                             \
+        switch (pl.vpt) {                                                                         \
+        case 1: return NAME##_sched<DT, RES, 1>(pl, p, st);                                       \
+        case 2: return NAME##_sched<DT, RES, 2>(pl, p, st);                                       \
+        case 4: return NAME##_sched<DT, RES, 4>(pl, p, st);                                       \
+        default: return NAME##_sched<DT, RES, 8>(pl, p, st);                                      \
+        }                                                                                         \
+    }                                                                                             \
+    template <int DT>                                                                             \
+    static cudaError_t NAME##_res(const Plan& pl, const Params& p, cudaStream_t st)               \
+    {                                                                                             \
+        return pl.res ? NAME##_vpt<DT, true>(pl, p, st) : NAME##_vpt<DT, false>(pl, p, st);      \
+    }                                                                                             \
+    cudaError_t NAME(const Plan& pl, const Params& p, cudaStream_t st)                            \
+    {                                                                                             \
+        switch (pl.dt) {                                                                          \
+        case DT_BF16: return NAME##_res<DT_BF16>(pl, p, st);                                      \
+        case DT_FP16: return NAME##_res<DT_FP16>(pl, p, st);                                      \
+        default: return NAME##_res<DT_F32>(pl, p, st);                                            \
+        }                                                                                         \
+    }
+
+}  // namespace rmsq

@@ -268,3 +268,16 @@ def test_fp4_half_step_invariant():
     s = e4[nv["block_scale"]]
     t = nv["t"]
     assert np.all(np.abs(s - t) <= np.maximum(np.exp2(np.floor(np.log2(np.maximum(t, 1e-300))) - 4), 2.0 ** -10))
+
+
+@pytest.mark.parametrize("sdt,tdt", [(oracle.BF16, torch.bfloat16), (oracle.FP16, torch.float16)])
+def test_fp8_rounded_scale_dtype(sdt, tdt):
+    w = W.config("fp8_residual", rows=32, hidden=512)
+    d = W.generate(w, seed=12)
+    args = (_bits(d["input"]), _bits(d["residual"]), _bits(d["gamma"]))
+    f32 = oracle.quant_fp8(*args, want_y=True)
+    low = oracle.quant_fp8(*args, scale_dtype=sdt, want_y=True, want_pre=True)
+    want = torch.from_numpy(f32["scale"]).to(tdt).float().numpy()
+    assert np.array_equal(low["scale"], want)
+    assert np.allclose(low["pre"], low["y"].astype(np.float64) / want[:, None].astype(np.float64))
+    assert np.array_equal(low["q"], oracle.e4m3_encode(low["pre"]))
