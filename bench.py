@@ -457,7 +457,10 @@ def run_report(args):
     torch.cuda.set_device(0)
     peak, _ = measured_peak()
     flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    only = set(args.only.split(",")) if args.only else None
     for name, rows, hidden in report_workloads():
+        if only and name not in only and "%s:%s:%s" % (name, rows, hidden) not in only:
+            continue
         w = W.config(name, rows=rows, hidden=hidden)
         d = W.generate(w, seed=0, device="cuda")
         x, r, g = d["input"], d["residual"], d["gamma"]
@@ -500,6 +503,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--report", action="store_true", help="per-workload GB/s lines")
     ap.add_argument("--report-reps", type=int, default=20)
+    ap.add_argument("--only", default="", help="--report: comma-separated workload names "
+                    "(or name:rows:hidden for one MXFP4 sweep point)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     args = ap.parse_args()

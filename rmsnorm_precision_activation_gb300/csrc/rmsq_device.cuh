@@ -436,8 +436,10 @@ __device__ __forceinline__ long long scale_offset(long long row, int sf, int nsf
 //   sum of squares  compensated (TwoSum) fp32 accumulation: hi + lo within ~2^-45 of the exact sum
 //   rstd            RN(1 / sqrt(sum / H + eps)) from one Newton step in float-float arithmetic
 //   y               RN(s * w * rstd) with s * w split exactly by an FMA
-//   y / scale       rounded to odd in fp32 (RN quotient, exact remainder, then RZ with a sticky
-//                   last bit), so that the E4M3 RNE conversion rounds the exact quotient
+//   y / scale       the correctly rounded fp32 quotient; when it lands exactly on an E4M3
+//                   boundary while the exact quotient does not (found from the exact remainder),
+//                   it moves one unit toward the exact value, so the E4M3 RNE conversion rounds
+//                   the exact quotient
 // FP4 codes see no such cancellation (the block scale is itself rounded, or a power of two applied
 // to y exactly), so the FP4 kernels and the amax pre-pass use a plain fp32 sum of squares and the
 // correctly rounded rsqrt of the rounded mean.
@@ -502,27 +504,97 @@ __device__ __forceinline__ float2 norm_mul2(float2 s, float2 w, float2 rstd)
     return fma2(hi, rstd, mul2(lo, rstd));
 }
 
-// Round-to-odd fp32 quotient y / d on a pair (d > 0), from inv = RN(1 / d) and nd = -d:
-// q = RN(y / d) by one correction step, r = y - q d exactly; then q moves one unit toward zero
-// when |y / d| < |q| and gets its last bit set whenever the division was inexact. The result
-// is RZ(y / d) with a sticky bit, so a later rounding to a format with at least two fewer bits
-// equals the correctly rounded exact quotient.
-__device__ __forceinline__ float ro_bits(float q, float r)
-{
-    const uint32_t b = __float_as_uint(q);
-    const uint32_t rb = __float_as_uint(r);
-    const bool inexact = ((rb << 1) != 0u) && ((b << 1) != 0u);
-    const uint32_t toward_zero = (rb ^ b) >> 31;
-    return __uint_as_float(inexact ? ((b - toward_zero) | 1u) : b);
-}
-
-__device__ __forceinline__ float2 div_odd2(float2 y, float2 nd, float2 inv)
+// RN(y / d) on a pair from inv = RN(1 / d) and nd = -d: one correction with the exact
+// remainder y - q0 d.
+__device__ __forceinline__ float2 div_rn2(float2 y, float2 nd, float2 inv)
 {
     const float2 q0 = mul2(y, inv);
-    const float2 q = fma2(fma2(q0, nd, y), inv, q0);
-    const float2 r = fma2(q, nd, y);
-    return make_float2(ro_bits(q.x, r.x), ro_bits(q.y, r.y));
+    return fma2(fma2(q0, nd, y), inv, q0);
 }
+
+// The correctly rounded fp32 quotient q can sit exactly on an E4M3 rounding boundary
+// (1.xxx1 x 2^e: the low 19 mantissa bits zero and bit 19 set) while the exact quotient lies just
+// off it; the E4M3 conversion would then break the tie to even instead of rounding the exact
+// value. tie_key is zero exactly for such candidates.
+__device__ __forceinline__ uint32_t tie_key(float q)
+{
+    return (__float_as_uint(q) & 0xFFFFFu) ^ 0x80000u;
+}
+
+// For a candidate, move q one unit toward the exact quotient y / d when the division was inexact,
+// so the E4M3 conversion rounds the exact value. nd = -d.
+__device__ __forceinline__ float untie(float q, float y, float nd)
+{
+    const float r = fmaf(q, nd, y);                          // y - q d, exact
+    if (tie_key(q) != 0u || r == 0.0f) return q;
+    const uint32_t b = __float_as_uint(q);
+    const bool away = ((__float_as_uint(r) ^ b) >> 31) == 0u;  // |y / d| > |q|
+    return __uint_as_float(away ? b + 1u : b - 1u);
+}
+
+// max |v| over the pairs of one vector, as a shallow tree.
+template <int NP>
+__device__ __forceinline__ float absmax_pairs(const float2 (&v)[NP])
+{
+    if constexpr (NP == 4) {
+        return max3(max3(fabsf(v[0].x), fabsf(v[0].y), fabsf(v[1].x)),
+                    max3(fabsf(v[1].y), fabsf(v[2].x), fabsf(v[2].y)),
+                    fmaxf(fabsf(v[3].x), fabsf(v[3].y)));
+    } else {
+        return max3(fabsf(v[0].x), fabsf(v[0].y), fmaxf(fabsf(v[1].x), fabsf(v[1].y)));
+    }
+}
+
+// w = fp32(gamma) + fp32(weight_offset) for this thread's vectors of the row. With up to four
+// vectors per thread w is kept as fp32 pairs for the CTA's lifetime; with more, gamma stays
+// packed and the offset is added per use.
+template <class E, int VPT, bool UNPACKED = (VPT <= 4)>
+struct GammaRegs;
+
+template <class E, int VPT>
+struct GammaRegs<E, VPT, true> {
+    static constexpr int NP = E::EPV / 2;
+    float2 w[VPT][NP];
+    __device__ __forceinline__ void load(const uint4* gp, int tid, int T, int nv, float2 off)
+    {
+#pragma unroll
+        for (int k = 0; k < VPT; ++k) {
+            const int v = tid + k * T;
+            const uint4 gv = v < nv ? __ldg(gp + v) : make_uint4(0, 0, 0, 0);
+            float2 f[NP];
+            E::pairs(gv, f);
+#pragma unroll
+            for (int j = 0; j < NP; ++j) w[k][j] = add2(f[j], off);
+        }
+    }
+    __device__ __forceinline__ void get(int k, float2 (&out)[NP]) const
+    {
+#pragma unroll
+        for (int j = 0; j < NP; ++j) out[j] = w[k][j];
+    }
+};
+
+template <class E, int VPT>
+struct GammaRegs<E, VPT, false> {
+    static constexpr int NP = E::EPV / 2;
+    uint4 g[VPT];
+    float2 off;
+    __device__ __forceinline__ void load(const uint4* gp, int tid, int T, int nv, float2 o)
+    {
+        off = o;
+#pragma unroll
+        for (int k = 0; k < VPT; ++k) {
+            const int v = tid + k * T;
+            g[k] = v < nv ? __ldg(gp + v) : make_uint4(0, 0, 0, 0);
+        }
+    }
+    __device__ __forceinline__ void get(int k, float2 (&out)[NP]) const
+    {
+        E::pairs(g[k], out);
+#pragma unroll
+        for (int j = 0; j < NP; ++j) out[j] = add2(out[j], off);
+    }
+};
 
 // Shared memory after the stage ring: [2][32] float2 sum-of-squares partials, [32] row amax,
 // [128] NVFP4 element factors gs / dec(s) indexed by the E4M3 block-scale code.
@@ -600,15 +672,10 @@ rmsq_row_kernel(const Params p)
         __syncthreads();
     }
 
-    // gamma stays packed in registers for the CTA's lifetime; the offset is added per use in
-    // fp32 (w = fp32(gamma) + fp32(weight_offset)).
-    uint4 g[VPT];
-#pragma unroll
-    for (int k = 0; k < VPT; ++k) {
-        const int v = tid + k * T;
-        g[k] = v < nv ? __ldg(static_cast<const uint4*>(p.gamma) + v) : make_uint4(0, 0, 0, 0);
-    }
     const float2 offset2 = splat(p.offset);
+    GammaRegs<E, VPT> G;
+    G.load(static_cast<const uint4*>(p.gamma), tid, T, nv, offset2);
+    const bool sw_exact = DT != DT_F32 && p.offset == 0.0f;   // s * gamma exact in fp32
     const float Hf = static_cast<float>(p.hidden);
     // lanes in the second reduction stage: the smallest power of two >= nwarps
     int red_lanes = 1;
@@ -724,31 +791,49 @@ rmsq_row_kernel(const Params p)
         const float2 rstd2 = splat(rstd);
 
         if constexpr (MODE == MODE_AMAX) {
+            // max |y| = rstd * max |s w| (rstd > 0, rounding is monotonic)
+            float mp = 0.0f;
 #pragma unroll
             for (int k = 0; k < VPT; ++k) {
-                float2 f[NP], gw[NP];
+                float2 f[NP], w[NP], sw[NP];
                 E::pairs(s[k], f);
-                E::pairs(g[k], gw);
+                G.get(k, w);
 #pragma unroll
-                for (int j = 0; j < NP; ++j) {
-                    const float2 y = mul2(mul2(f[j], add2(gw[j], offset2)), rstd2);
-                    run_max = max3(run_max, fabsf(y.x), fabsf(y.y));
-                }
+                for (int j = 0; j < NP; ++j) sw[j] = mul2(f[j], w[j]);
+                mp = fmaxf(mp, absmax_pairs(sw));
             }
+            if (mp > 0.0f) run_max = fmaxf(run_max, __fmul_rn(mp, rstd));
         } else if constexpr (MODE == MODE_FP8) {
             // ---- y, row amax, scale, E4M3 codes ----------------------------------------------
+            // With 16-bit inputs and weight_offset 0, s * w is exact and y = RN(RN(s w) rstd) is
+            // already the correctly rounded product; otherwise the FMA split forms it.
             float2 y[KEEP_Y ? VPT : 1][NP];
             float amax = 0.0f;
+            if (sw_exact) {
 #pragma unroll
-            for (int k = 0; k < VPT; ++k) {
-                float2 f[NP], gw[NP];
-                E::pairs(s[k], f);
-                E::pairs(g[k], gw);
+                for (int k = 0; k < VPT; ++k) {
+                    float2 f[NP], w[NP], yy[NP];
+                    E::pairs(s[k], f);
+                    G.get(k, w);
 #pragma unroll
-                for (int j = 0; j < NP; ++j) {
-                    const float2 yy = norm_mul2(f[j], add2(gw[j], offset2), rstd2);
-                    if constexpr (KEEP_Y) y[k][j] = yy;
-                    amax = max3(amax, fabsf(yy.x), fabsf(yy.y));
+                    for (int j = 0; j < NP; ++j) {
+                        yy[j] = mul2(mul2(f[j], w[j]), rstd2);
+                        if constexpr (KEEP_Y) y[k][j] = yy[j];
+                    }
+                    amax = fmaxf(amax, absmax_pairs(yy));
+                }
+            } else {
+#pragma unroll
+                for (int k = 0; k < VPT; ++k) {
+                    float2 f[NP], w[NP], yy[NP];
+                    E::pairs(s[k], f);
+                    G.get(k, w);
+#pragma unroll
+                    for (int j = 0; j < NP; ++j) {
+                        yy[j] = norm_mul2(f[j], w[j], rstd2);
+                        if constexpr (KEEP_Y) y[k][j] = yy[j];
+                    }
+                    amax = fmaxf(amax, absmax_pairs(yy));
                 }
             }
             amax = warp_max(amax);
@@ -785,18 +870,30 @@ rmsq_row_kernel(const Params p)
 #pragma unroll
                     for (int j = 0; j < NP; ++j) yk[j] = y[k][j];
                 } else {
-                    float2 f[NP], gw[NP];
+                    float2 f[NP], w[NP];
                     E::pairs(s[k], f);
-                    E::pairs(g[k], gw);
+                    G.get(k, w);
 #pragma unroll
-                    for (int j = 0; j < NP; ++j) yk[j] = norm_mul2(f[j], add2(gw[j], offset2), rstd2);
+                    for (int j = 0; j < NP; ++j)
+                        yk[j] = sw_exact ? mul2(mul2(f[j], w[j]), rstd2) : norm_mul2(f[j], w[j], rstd2);
+                }
+                float2 q[NP];
+                uint32_t key = 0xFFFFFFFFu;
+#pragma unroll
+                for (int j = 0; j < NP; ++j) {
+                    q[j] = div_rn2(yk[j], nd2, inv2);
+                    key = min(key, min(tie_key(q[j].x), tie_key(q[j].y)));
+                }
+                if (key == 0u) {           // rare: a quotient sits on an E4M3 boundary
+#pragma unroll
+                    for (int j = 0; j < NP; ++j) {
+                        q[j].x = untie(q[j].x, yk[j].x, nd2.x);
+                        q[j].y = untie(q[j].y, yk[j].y, nd2.y);
+                    }
                 }
                 uint32_t c[NP];
 #pragma unroll
-                for (int j = 0; j < NP; ++j) {
-                    const float2 q = div_odd2(yk[j], nd2, inv2);
-                    c[j] = zero_row ? 0u : cvt_e4m3x2(q.x, q.y);
-                }
+                for (int j = 0; j < NP; ++j) c[j] = zero_row ? 0u : cvt_e4m3x2(q[j].x, q[j].y);
                 if constexpr (EPV == 8) {
                     st_v2(outp + v * 8, c[0] | (c[1] << 16), c[2] | (c[3] << 16));
                 } else {
@@ -805,33 +902,35 @@ rmsq_row_kernel(const Params p)
             }
         } else {
             // ---- FP4: per-block amax across GROUP adjacent lanes, scale, E2M1 ---------------
+            // The block max of y is rstd * max |s w|, and the codes are E2M1(s w * rstd * factor)
+            // with rstd folded into the block factor: for MXFP4 the factor is a power of two, so
+            // the codes equal E2M1(RN(s w rstd) * 2^(127 - e)) whenever s w is exact.
             unsigned char* outp = static_cast<unsigned char*>(p.out) + row * (p.hidden / 2);
             unsigned char* sp = static_cast<unsigned char*>(p.scale_out);
 #pragma unroll
             for (int k = 0; k < VPT; ++k) {
                 const int v = tid + k * T;
-                float2 y[NP];
+                float2 sw[NP];
                 float m = 0.0f;
                 {
-                    float2 f[NP], gw[NP];
+                    float2 f[NP], w[NP];
                     E::pairs(s[k], f);
-                    E::pairs(g[k], gw);
+                    G.get(k, w);
 #pragma unroll
-                    for (int j = 0; j < NP; ++j) {
-                        y[j] = mul2(mul2(f[j], add2(gw[j], offset2)), rstd2);
-                        m = max3(m, fabsf(y[j].x), fabsf(y[j].y));
-                    }
+                    for (int j = 0; j < NP; ++j) sw[j] = mul2(f[j], w[j]);
+                    m = absmax_pairs(sw);
                 }
 #pragma unroll
                 for (int o = 1; o < GROUP; o <<= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+                const float a = m > 0.0f ? __fmul_rn(m, rstd) : 0.0f;      // block max |y|
                 float factor;
                 uint32_t code;
                 if constexpr (MODE == MODE_NVFP4) {
-                    const float t = fminf(__fmul_rn(m, gs_over_6), 448.0f);
+                    const float t = fminf(__fmul_rn(a, gs_over_6), 448.0f);
                     code = cvt_e4m3x2(t, 0.0f) & 0xFFu;
                     factor = nv_factor[code & 0x7Fu];
                 } else {
-                    code = ue8m0_code(m);
+                    code = ue8m0_code(a);
                     factor = ue8m0_inv_factor(code);
                 }
                 if (v >= nv) continue;
@@ -839,12 +938,12 @@ rmsq_row_kernel(const Params p)
                     sp[scale_offset(row, v / GROUP, p.nsf, p.swizzled, p.k_tiles)] =
                         static_cast<unsigned char>(code);
                 const bool zero_block = !(factor > 0.0f);
-                const float2 f2 = splat(factor);
+                const float2 f2 = splat(zero_block ? 0.0f : __fmul_rn(factor, rstd));
                 if constexpr (EPV == 8) {
                     float q[8];
 #pragma unroll
                     for (int j = 0; j < 4; ++j) {
-                        const float2 qq = mul2(y[j], f2);
+                        const float2 qq = mul2(sw[j], f2);
                         q[2 * j] = qq.x;
                         q[2 * j + 1] = qq.y;
                     }
@@ -853,7 +952,7 @@ rmsq_row_kernel(const Params p)
                     float q[4];
 #pragma unroll
                     for (int j = 0; j < 2; ++j) {
-                        const float2 qq = mul2(y[j], f2);
+                        const float2 qq = mul2(sw[j], f2);
                         q[2 * j] = qq.x;
                         q[2 * j + 1] = qq.y;
                     }
