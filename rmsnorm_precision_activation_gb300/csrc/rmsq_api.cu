@@ -116,9 +116,10 @@ cudaError_t run_kernel(const void* fn, const Plan& pl, const Params& p, cudaStre
 static int elems_per_vec(int dt) { return dt == DT_F32 ? 4 : 8; }
 
 // Pick vectors per thread, CTA size, schedule, ring depth and residency for one call.
-// Measured on GB300: small CTAs (about 128 threads, 4 vectors of 16 bytes each per thread per
-// row), a two-row ring each, and as many CTAs per SM as shared memory and registers allow keep
-// several rows in computation per SM while the next ones stream in.
+// From on-GPU sweeps (GB300): each thread takes the power of two nearest nv / 128 vectors of 16
+// bytes per row (nv / 256 for FP4 with a residual; FP8 at most 4, so y stays in registers); a
+// two-row ring per CTA; FP4 kernels with a residual run best with few CTAs per SM (3), FP4
+// kernels without one and the FP8 kernel with more (8 and 6).
 static bool make_plan(int mode, int dt, bool res, int hidden, const DeviceInfo& di, Plan& pl)
 {
     const int nv = hidden / elems_per_vec(dt);
@@ -127,9 +128,12 @@ static bool make_plan(int mode, int dt, bool res, int hidden, const DeviceInfo& 
     pl.res = res;
     int vpt = g_tune_vpt.load();
     if (vpt == 0) {
-        vpt = 4;
+        // vectors per thread: the power of two nearest nv / target threads
+        const int target = (mode != MODE_FP8 && res) ? 256 : 128;
+        vpt = 1;
+        while (vpt < 8 && 2 * nv > 3 * target * vpt) vpt *= 2;
+        if (mode == MODE_FP8 && vpt > 4) vpt = 4;
         while (vpt < 8 && (nv + vpt - 1) / vpt > 512) vpt *= 2;
-        while (vpt > 1 && (nv + vpt - 1) / vpt < 64) vpt /= 2;
     }
     int threads = ((nv + vpt - 1) / vpt + 31) / 32 * 32;
     if (threads > 512) return false;
@@ -142,7 +146,11 @@ static bool make_plan(int mode, int dt, bool res, int hidden, const DeviceInfo& 
     const bool pipe_fits = 2 * stage + red_bytes + 2 * 8 <= di.smem_optin;
     pl.sched = (forced == SCHED_REG || !pipe_fits) ? SCHED_REG : SCHED_PIPE;
     pl.ctas_per_sm = g_tune_ctas.load();
-    if (pl.ctas_per_sm == 0) pl.ctas_per_sm = 16;
+    if (pl.ctas_per_sm == 0) {
+        if (mode == MODE_FP8) pl.ctas_per_sm = 6;
+        else if (!res) pl.ctas_per_sm = 8;
+        else pl.ctas_per_sm = 3;
+    }
     if (pl.sched == SCHED_PIPE) {
         int stages = g_tune_stages.load();
         if (stages == 0) stages = 2;
@@ -207,6 +215,7 @@ static rmsq_status launch(int mode, Params& p, bool res, int dtype, const Device
 {
     Plan pl;
     if (!make_plan(mode, dtype, res, p.hidden, di, pl)) return RMSQ_ERR_SHAPE;
+    pl.w16 = dtype != DT_F32 && p.offset == 0.0f;
     p.stages = pl.stages;
     cudaError_t e;
     switch (mode) {

@@ -236,6 +236,27 @@ template <int DT> struct Elem;
 
 template <> struct Elem<DT_BF16> {
     static constexpr int EPV = 8;
+    // Exact products of the two bf16 halves of a and b (mixed-precision FMA with a zero addend:
+    // a 16-bit by 16-bit product is exact in fp32).
+    static __device__ __forceinline__ float2 mul_halves(uint32_t a, uint32_t b)
+    {
+        float2 r;
+        asm("{\n\t.reg .b16 a0, a1, b0, b1;\n\tmov.b32 {a0, a1}, %2;\n\tmov.b32 {b0, b1}, %3;\n\t"
+            "fma.rn.f32.bf16 %0, a0, b0, 0f80000000;\n\tfma.rn.f32.bf16 %1, a1, b1, 0f80000000;\n\t}"
+            : "=f"(r.x), "=f"(r.y)
+            : "r"(a), "r"(b));
+        return r;
+    }
+    // acc + (halves of a)^2, one rounding each.
+    static __device__ __forceinline__ float2 sq_acc(uint32_t a, float2 acc)
+    {
+        float2 r;
+        asm("{\n\t.reg .b16 a0, a1;\n\tmov.b32 {a0, a1}, %2;\n\t"
+            "fma.rn.f32.bf16 %0, a0, a0, %3;\n\tfma.rn.f32.bf16 %1, a1, a1, %4;\n\t}"
+            : "=f"(r.x), "=f"(r.y)
+            : "r"(a), "f"(acc.x), "f"(acc.y));
+        return r;
+    }
     // Element pairs (2j, 2j+1) as float2, exact.
     static __device__ __forceinline__ void pairs(const uint4& v, float2 (&f)[4])
     {
@@ -267,6 +288,24 @@ template <> struct Elem<DT_BF16> {
 
 template <> struct Elem<DT_FP16> {
     static constexpr int EPV = 8;
+    static __device__ __forceinline__ float2 mul_halves(uint32_t a, uint32_t b)
+    {
+        float2 r;
+        asm("{\n\t.reg .b16 a0, a1, b0, b1;\n\tmov.b32 {a0, a1}, %2;\n\tmov.b32 {b0, b1}, %3;\n\t"
+            "fma.rn.f32.f16 %0, a0, b0, 0f80000000;\n\tfma.rn.f32.f16 %1, a1, b1, 0f80000000;\n\t}"
+            : "=f"(r.x), "=f"(r.y)
+            : "r"(a), "r"(b));
+        return r;
+    }
+    static __device__ __forceinline__ float2 sq_acc(uint32_t a, float2 acc)
+    {
+        float2 r;
+        asm("{\n\t.reg .b16 a0, a1;\n\tmov.b32 {a0, a1}, %2;\n\t"
+            "fma.rn.f32.f16 %0, a0, a0, %3;\n\tfma.rn.f32.f16 %1, a1, a1, %4;\n\t}"
+            : "=f"(r.x), "=f"(r.y)
+            : "r"(a), "f"(acc.x), "f"(acc.y));
+        return r;
+    }
     static __device__ __forceinline__ void pairs(const uint4& v, float2 (&f)[4])
     {
         const uint32_t w[4] = {v.x, v.y, v.z, v.w};
@@ -307,6 +346,9 @@ template <> struct Elem<DT_FP16> {
 
 template <> struct Elem<DT_F32> {
     static constexpr int EPV = 4;
+    // (not used: fp32 rows always take the unpacked path)
+    static __device__ __forceinline__ float2 mul_halves(uint32_t, uint32_t) { return make_float2(0.f, 0.f); }
+    static __device__ __forceinline__ float2 sq_acc(uint32_t, float2 acc) { return acc; }
     static __device__ __forceinline__ void pairs(const uint4& v, float2 (&f)[2])
     {
         f[0] = make_float2(__uint_as_float(v.x), __uint_as_float(v.y));
@@ -331,46 +373,17 @@ template <> struct Elem<DT_F32> {
 };
 
 // Packed fp32 pairs (Blackwell f32x2 instructions: two IEEE round-to-nearest operations per
-// instruction).
-__device__ __forceinline__ float2 add2(float2 a, float2 b)
-{
-    float2 r;
-    asm("{\n\t.reg .b64 pa, pb, pd;\n\tmov.b64 pa, {%2, %3};\n\tmov.b64 pb, {%4, %5};\n\t"
-        "add.rn.f32x2 pd, pa, pb;\n\tmov.b64 {%0, %1}, pd;\n\t}"
-        : "=f"(r.x), "=f"(r.y)
-        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
-    return r;
-}
+// instruction), through CUDA's float2 intrinsics so the compiler can keep pairs in register pairs.
+__device__ __forceinline__ float2 add2(float2 a, float2 b) { return __fadd2_rn(a, b); }
 
 __device__ __forceinline__ float2 sub2(float2 a, float2 b)
 {
-    float2 r;
-    asm("{\n\t.reg .b64 pa, pb, pd;\n\tmov.b64 pa, {%2, %3};\n\tmov.b64 pb, {%4, %5};\n\t"
-        "sub.rn.f32x2 pd, pa, pb;\n\tmov.b64 {%0, %1}, pd;\n\t}"
-        : "=f"(r.x), "=f"(r.y)
-        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
-    return r;
+    return __fadd2_rn(a, make_float2(-b.x, -b.y));
 }
 
-__device__ __forceinline__ float2 mul2(float2 a, float2 b)
-{
-    float2 r;
-    asm("{\n\t.reg .b64 pa, pb, pd;\n\tmov.b64 pa, {%2, %3};\n\tmov.b64 pb, {%4, %5};\n\t"
-        "mul.rn.f32x2 pd, pa, pb;\n\tmov.b64 {%0, %1}, pd;\n\t}"
-        : "=f"(r.x), "=f"(r.y)
-        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
-    return r;
-}
+__device__ __forceinline__ float2 mul2(float2 a, float2 b) { return __fmul2_rn(a, b); }
 
-__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c)
-{
-    float2 r;
-    asm("{\n\t.reg .b64 pa, pb, pc, pd;\n\tmov.b64 pa, {%2, %3};\n\tmov.b64 pb, {%4, %5};\n\t"
-        "mov.b64 pc, {%6, %7};\n\tfma.rn.f32x2 pd, pa, pb, pc;\n\tmov.b64 {%0, %1}, pd;\n\t}"
-        : "=f"(r.x), "=f"(r.y)
-        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
-    return r;
-}
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) { return __ffma2_rn(a, b, c); }
 
 __device__ __forceinline__ float max3(float a, float b, float c)
 {
@@ -414,14 +427,6 @@ __device__ __forceinline__ uint32_t ue8m0_code(float a)
 __device__ __forceinline__ float ue8m0_inv_factor(uint32_t code)
 {
     return code == 0u ? 0.0f : __uint_as_float((254u - code) << 23);
-}
-
-__device__ __forceinline__ long long scale_offset(long long row, int sf, int nsf, int swizzled,
-                                                  int k_tiles)
-{
-    if (!swizzled) return row * nsf + sf;
-    return (row >> 7) * (static_cast<long long>(k_tiles) * 512) + (sf >> 2) * 512 +
-           (row & 31) * 16 + ((row & 127) >> 5) * 4 + (sf & 3);
 }
 
 // ------------------------------------------------------------------------------------------
@@ -493,6 +498,21 @@ __device__ __forceinline__ float rstd_from_sum(FF ss, float H, float eps)
     const float t_hi = __fmul_rn(m.hi, p_hi);
     const float t_lo = __fadd_rn(fmaf(m.hi, p_hi, -t_hi), fmaf(m.hi, p_lo, __fmul_rn(m.lo, p_hi)));
     const float e = __fsub_rn(__fsub_rn(1.0f, t_hi), t_lo);   // 1 - m r0^2, t_hi ~ 1 so exact
+    return __fadd_rn(r0, __fmul_rn(__fmul_rn(r0, 0.5f), e));
+}
+
+// As rstd_from_sum for a power-of-two H (inv_h = 1 / H exactly, so the mean is exact).
+__device__ __forceinline__ float rstd_from_sum_pow2(FF ss, float inv_h, float eps)
+{
+    FF m = two_sum(__fmul_rn(ss.hi, inv_h), eps);
+    m.lo = __fadd_rn(m.lo, __fmul_rn(ss.lo, inv_h));
+    if (!(m.hi > 0.0f)) return __int_as_float(0x7F800000);
+    const float r0 = rsqrtf(m.hi);
+    const float p_hi = __fmul_rn(r0, r0);
+    const float p_lo = fmaf(r0, r0, -p_hi);
+    const float t_hi = __fmul_rn(m.hi, p_hi);
+    const float t_lo = __fadd_rn(fmaf(m.hi, p_hi, -t_hi), fmaf(m.hi, p_lo, __fmul_rn(m.lo, p_hi)));
+    const float e = __fsub_rn(__fsub_rn(1.0f, t_hi), t_lo);
     return __fadd_rn(r0, __fmul_rn(__fmul_rn(r0, 0.5f), e));
 }
 
@@ -604,7 +624,9 @@ constexpr int kRedFloats = 2 * 32 * 2 + 32 + 128;
 // The kernel
 // ------------------------------------------------------------------------------------------
 
-template <int DT, bool RES, int MODE, int VPT, int SCHED>
+// W16: 16-bit input with weight_offset 0, so w = gamma is a 16-bit value and s * w, s^2 are
+// exact products formed straight from packed halves by mixed-precision FMA (no unpacking).
+template <int DT, bool RES, int MODE, int VPT, int SCHED, bool W16>
 __global__ void __launch_bounds__(512, 1)
 rmsq_row_kernel(const Params p)
 {
@@ -673,24 +695,29 @@ rmsq_row_kernel(const Params p)
     }
 
     const float2 offset2 = splat(p.offset);
-    GammaRegs<E, VPT> G;
+    GammaRegs<E, VPT, !W16 && VPT <= 4> G;
     G.load(static_cast<const uint4*>(p.gamma), tid, T, nv, offset2);
-    const bool sw_exact = DT != DT_F32 && p.offset == 0.0f;   // s * gamma exact in fp32
+    constexpr bool sw_exact = W16;                            // s * gamma exact in fp32
     const float Hf = static_cast<float>(p.hidden);
     // lanes in the second reduction stage: the smallest power of two >= nwarps
     int red_lanes = 1;
     while (red_lanes < nwarps) red_lanes <<= 1;
 
+    // 1 / H: exact when H is a power of two (the FP8 exact path then skips the division)
+    const bool h_pow2 = (p.hidden & (p.hidden - 1)) == 0;
+    const float inv_h = __frcp_rn(Hf);
+
     float run_max = 0.0f;   // MODE_AMAX: max |y| over this thread's share of the CTA's rows
-    long long it = 0;
-    for (long long row = blockIdx.x; row < p.rows; row += gridDim.x, ++it) {
+    int stage = 0;          // ring slot of this row, and the mbarrier phase parity to wait for
+    uint32_t parity = 0;
+    int rbuf = 0;           // which of the two sum-of-squares reduction buffers this row uses
+    for (long long row = blockIdx.x; row < p.rows; row += gridDim.x) {
+        const uint4* __restrict__ xrow = xg + row * nv;
+        const uint4* __restrict__ rrow = RES ? rg + row * nv : nullptr;
         // ---- load the row, add the residual, write residual_output, sum of squares ----------
         bool timed_out = false;
         uint32_t stage_addr = 0;
-        int stage = 0;
         if constexpr (SCHED == SCHED_PIPE) {
-            stage = static_cast<int>(it % S);
-            const uint32_t parity = static_cast<uint32_t>((it / S) & 1);
             stage_addr = smem_u32(smem + static_cast<size_t>(stage) * stage_bytes);
             timed_out = !mbar_wait_bounded(smem_u32(&bars[stage]), parity, p.timeout_ns);
         }
@@ -706,8 +733,8 @@ rmsq_row_kernel(const Params p)
                     xv = ld_shared_v4(stage_addr + v * 16u);
                     if constexpr (RES) rv = ld_shared_v4(stage_addr + row_bytes + v * 16u);
                 } else {
-                    xv = ld_stream_v4(xg + row * nv + v);
-                    if constexpr (RES) rv = ld_stream_v4(rg + row * nv + v);
+                    xv = ld_stream_v4(xrow + v);
+                    if constexpr (RES) rv = ld_stream_v4(rrow + v);
                 }
                 if constexpr (RES) {
                     s[k] = E::add(xv, rv);
@@ -715,33 +742,54 @@ rmsq_row_kernel(const Params p)
                 } else {
                     s[k] = xv;
                 }
-                float2 f[NP];
-                E::pairs(s[k], f);
-#pragma unroll
-                for (int j = 0; j < NP; ++j) {
+                if constexpr (W16) {
+                    const uint32_t sv[4] = {s[k].x, s[k].y, s[k].z, s[k].w};
                     if constexpr (EXACT) {
-                        const float2 sq = mul2(f[j], f[j]);          // exact for 16-bit inputs
-                        float2 t, e;
-                        two_sum2(acc_hi, sq, t, e);
-                        acc_hi = t;
-                        acc_lo = add2(acc_lo, e);
-                        if constexpr (DT == DT_F32)
-                            acc_lo = add2(acc_lo, fma2(f[j], f[j], make_float2(-sq.x, -sq.y)));
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            const float2 sq = E::mul_halves(sv[j], sv[j]);   // exact squares
+                            float2 t, e;
+                            two_sum2(acc_hi, sq, t, e);
+                            acc_hi = t;
+                            acc_lo = add2(acc_lo, e);
+                        }
                     } else {
-                        acc_hi = fma2(f[j], f[j], acc_hi);
+                        // two independent accumulator pairs shorten the dependency chain
+                        acc_hi = E::sq_acc(sv[0], acc_hi);
+                        acc_lo = E::sq_acc(sv[1], acc_lo);
+                        acc_hi = E::sq_acc(sv[2], acc_hi);
+                        acc_lo = E::sq_acc(sv[3], acc_lo);
+                    }
+                } else {
+                    float2 f[NP];
+                    E::pairs(s[k], f);
+#pragma unroll
+                    for (int j = 0; j < NP; ++j) {
+                        if constexpr (EXACT) {
+                            const float2 sq = mul2(f[j], f[j]);          // exact for 16-bit inputs
+                            float2 t, e;
+                            two_sum2(acc_hi, sq, t, e);
+                            acc_hi = t;
+                            acc_lo = add2(acc_lo, e);
+                            if constexpr (DT == DT_F32)
+                                acc_lo = add2(acc_lo, fma2(f[j], f[j], make_float2(-sq.x, -sq.y)));
+                        } else {
+                            acc_hi = fma2(f[j], f[j], acc_hi);
+                        }
                     }
                 }
             }
         }
         // ---- CTA reduction of the sum of squares -> rstd ----------------------------------
-        float2* red_ss = red_ss_all + (it & 1) * 32;
+        float2* red_ss = red_ss_all + rbuf * 32;
+        rbuf ^= 1;
         FF ss;
         if constexpr (EXACT) {
             ss = ff_add(FF{acc_hi.x, acc_lo.x}, FF{acc_hi.y, acc_lo.y});
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) ss = ff_add(ss, shfl_xor_ff(ss, o));
         } else {
-            ss = FF{warp_sum(__fadd_rn(acc_hi.x, acc_hi.y)), 0.0f};
+            ss = FF{warp_sum(__fadd_rn(__fadd_rn(acc_hi.x, acc_hi.y), __fadd_rn(acc_lo.x, acc_lo.y))), 0.0f};
         }
         if (lane == 0) red_ss[warp] = make_float2(ss.hi, ss.lo);
         if (__syncthreads_or(timed_out)) {
@@ -749,12 +797,16 @@ rmsq_row_kernel(const Params p)
                 if (tid == 0) {
                     atomicOr(p.err, ERRF_WAIT_TIMEOUT);
                     // let the copies already issued for later rows land (bounded) before exit
+                    int js = stage;
+                    uint32_t jp = parity;
                     for (int j = 1; j < S; ++j) {
                         const long long jrow = row + static_cast<long long>(j) * gridDim.x;
                         if (jrow >= p.rows) break;
-                        const long long jit = it + j;
-                        mbar_wait_bounded(smem_u32(&bars[jit % S]),
-                                          static_cast<uint32_t>((jit / S) & 1), p.timeout_ns);
+                        if (++js == S) {
+                            js = 0;
+                            jp ^= 1u;
+                        }
+                        mbar_wait_bounded(smem_u32(&bars[js]), jp, p.timeout_ns);
                     }
                 }
             }
@@ -777,29 +829,45 @@ rmsq_row_kernel(const Params p)
             const float2 part = lane < nwarps ? red_ss[lane] : make_float2(0.0f, 0.0f);
             if constexpr (EXACT) {
                 FF t{part.x, part.y};
-                for (int o = red_lanes >> 1; o > 0; o >>= 1) t = ff_add(t, shfl_xor_ff(t, o));
+#pragma unroll
+                for (int o = 8; o > 0; o >>= 1)
+                    if (o < red_lanes) t = ff_add(t, shfl_xor_ff(t, o));
                 t.hi = __shfl_sync(0xFFFFFFFFu, t.hi, 0);
                 t.lo = __shfl_sync(0xFFFFFFFFu, t.lo, 0);
-                rstd = rstd_from_sum(t, Hf, p.eps);
+                rstd = h_pow2 ? rstd_from_sum_pow2(t, inv_h, p.eps) : rstd_from_sum(t, Hf, p.eps);
             } else {
                 float t = part.x;
-                for (int o = red_lanes >> 1; o > 0; o >>= 1) t += __shfl_xor_sync(0xFFFFFFFFu, t, o);
+#pragma unroll
+                for (int o = 8; o > 0; o >>= 1)
+                    if (o < red_lanes) t += __shfl_xor_sync(0xFFFFFFFFu, t, o);
                 t = __shfl_sync(0xFFFFFFFFu, t, 0);
-                rstd = __frsqrt_rn(__fadd_rn(__fdiv_rn(t, Hf), p.eps));
+                rstd = __frsqrt_rn(__fadd_rn(__fmul_rn(t, inv_h), p.eps));
             }
         }
         const float2 rstd2 = splat(rstd);
+        // s * w for the pairs of vector k (exact when W16)
+        auto sw_pairs = [&](int k, float2 (&out)[NP]) {
+            if constexpr (W16) {
+                const uint32_t sv[4] = {s[k].x, s[k].y, s[k].z, s[k].w};
+                const uint32_t gv[4] = {G.g[k].x, G.g[k].y, G.g[k].z, G.g[k].w};
+#pragma unroll
+                for (int j = 0; j < NP; ++j) out[j] = E::mul_halves(sv[j], gv[j]);
+            } else {
+                float2 f[NP], w[NP];
+                E::pairs(s[k], f);
+                G.get(k, w);
+#pragma unroll
+                for (int j = 0; j < NP; ++j) out[j] = mul2(f[j], w[j]);
+            }
+        };
 
         if constexpr (MODE == MODE_AMAX) {
             // max |y| = rstd * max |s w| (rstd > 0, rounding is monotonic)
             float mp = 0.0f;
 #pragma unroll
             for (int k = 0; k < VPT; ++k) {
-                float2 f[NP], w[NP], sw[NP];
-                E::pairs(s[k], f);
-                G.get(k, w);
-#pragma unroll
-                for (int j = 0; j < NP; ++j) sw[j] = mul2(f[j], w[j]);
+                float2 sw[NP];
+                sw_pairs(k, sw);
                 mp = fmaxf(mp, absmax_pairs(sw));
             }
             if (mp > 0.0f) run_max = fmaxf(run_max, __fmul_rn(mp, rstd));
@@ -809,15 +877,14 @@ rmsq_row_kernel(const Params p)
             // already the correctly rounded product; otherwise the FMA split forms it.
             float2 y[KEEP_Y ? VPT : 1][NP];
             float amax = 0.0f;
-            if (sw_exact) {
+            if constexpr (sw_exact) {
 #pragma unroll
                 for (int k = 0; k < VPT; ++k) {
-                    float2 f[NP], w[NP], yy[NP];
-                    E::pairs(s[k], f);
-                    G.get(k, w);
+                    float2 yy[NP];
+                    sw_pairs(k, yy);
 #pragma unroll
                     for (int j = 0; j < NP; ++j) {
-                        yy[j] = mul2(mul2(f[j], w[j]), rstd2);
+                        yy[j] = mul2(yy[j], rstd2);
                         if constexpr (KEEP_Y) y[k][j] = yy[j];
                     }
                     amax = fmaxf(amax, absmax_pairs(yy));
@@ -840,8 +907,9 @@ rmsq_row_kernel(const Params p)
             if (lane == 0) red_max[warp] = amax;
             __syncthreads();
             amax = lane < nwarps ? red_max[lane] : 0.0f;
-            for (int o = red_lanes >> 1; o > 0; o >>= 1)
-                amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
+#pragma unroll
+            for (int o = 8; o > 0; o >>= 1)
+                if (o < red_lanes) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
             amax = __shfl_sync(0xFFFFFFFFu, amax, 0);
             float scale = __fdiv_rn(fminf(amax, p.scale_ub), 448.0f);
             if (p.scale_dtype == DT_BF16) {
@@ -869,13 +937,16 @@ rmsq_row_kernel(const Params p)
                 if constexpr (KEEP_Y) {
 #pragma unroll
                     for (int j = 0; j < NP; ++j) yk[j] = y[k][j];
+                } else if constexpr (sw_exact) {
+                    sw_pairs(k, yk);
+#pragma unroll
+                    for (int j = 0; j < NP; ++j) yk[j] = mul2(yk[j], rstd2);
                 } else {
                     float2 f[NP], w[NP];
                     E::pairs(s[k], f);
                     G.get(k, w);
 #pragma unroll
-                    for (int j = 0; j < NP; ++j)
-                        yk[j] = sw_exact ? mul2(mul2(f[j], w[j]), rstd2) : norm_mul2(f[j], w[j], rstd2);
+                    for (int j = 0; j < NP; ++j) yk[j] = norm_mul2(f[j], w[j], rstd2);
                 }
                 float2 q[NP];
                 uint32_t key = 0xFFFFFFFFu;
@@ -906,20 +977,19 @@ rmsq_row_kernel(const Params p)
             // with rstd folded into the block factor: for MXFP4 the factor is a power of two, so
             // the codes equal E2M1(RN(s w rstd) * 2^(127 - e)) whenever s w is exact.
             unsigned char* outp = static_cast<unsigned char*>(p.out) + row * (p.hidden / 2);
-            unsigned char* sp = static_cast<unsigned char*>(p.scale_out);
+            // scale byte of block sf sits at sp_row + col(sf): row-major sp + row * nsf + sf, or
+            // the swizzled 128x4 tile position (row part here, scale part per block)
+            unsigned char* sp_row = static_cast<unsigned char*>(p.scale_out) +
+                (p.swizzled ? (row >> 7) * (static_cast<long long>(p.k_tiles) * 512) +
+                                  (row & 31) * 16 + ((row & 127) >> 5) * 4
+                            : row * p.nsf);
 #pragma unroll
             for (int k = 0; k < VPT; ++k) {
                 const int v = tid + k * T;
                 float2 sw[NP];
                 float m = 0.0f;
-                {
-                    float2 f[NP], w[NP];
-                    E::pairs(s[k], f);
-                    G.get(k, w);
-#pragma unroll
-                    for (int j = 0; j < NP; ++j) sw[j] = mul2(f[j], w[j]);
-                    m = absmax_pairs(sw);
-                }
+                sw_pairs(k, sw);
+                m = absmax_pairs(sw);
 #pragma unroll
                 for (int o = 1; o < GROUP; o <<= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
                 const float a = m > 0.0f ? __fmul_rn(m, rstd) : 0.0f;      // block max |y|
@@ -935,8 +1005,10 @@ rmsq_row_kernel(const Params p)
                 }
                 if (v >= nv) continue;
                 if ((v & (GROUP - 1)) == 0)
-                    sp[scale_offset(row, v / GROUP, p.nsf, p.swizzled, p.k_tiles)] =
-                        static_cast<unsigned char>(code);
+                {
+                    const int sf = v / GROUP;
+                    sp_row[p.swizzled ? (sf >> 2) * 512 + (sf & 3) : sf] = static_cast<unsigned char>(code);
+                }
                 const bool zero_block = !(factor > 0.0f);
                 const float2 f2 = splat(zero_block ? 0.0f : __fmul_rn(factor, rstd));
                 if constexpr (EPV == 8) {
@@ -958,6 +1030,12 @@ rmsq_row_kernel(const Params p)
                     }
                     st_u16(outp + v * 2, static_cast<uint16_t>(zero_block ? 0u : cvt_e2m1x4(q)));
                 }
+            }
+        }
+        if constexpr (SCHED == SCHED_PIPE) {
+            if (++stage == S) {
+                stage = 0;
+                parity ^= 1u;
             }
         }
     }

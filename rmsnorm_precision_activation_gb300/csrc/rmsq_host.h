@@ -19,6 +19,7 @@ struct Plan {
     int stages;        // SCHED_PIPE ring depth
     int smem;          // dynamic shared memory bytes
     int ctas_per_sm;   // cap on resident CTAs per SM (0: occupancy limit)
+    bool w16;          // 16-bit input and weight_offset 0: products from packed halves
 };
 
 // Launch `fn` (a rmsq_row_kernel instantiation) with the plan: sets the dynamic shared memory
@@ -33,17 +34,26 @@ cudaError_t dispatch_amax(const Plan& plan, const Params& p, cudaStream_t stream
 
 // Instantiates the dispatch switch for one mode inside a .cu file.
 #define RMSQ_DEFINE_DISPATCH(NAME, MODE)                                                         \
-    template <int DT, bool RES, int VPT, int SCHED>                                               \
+    template <int DT, bool RES, int VPT, int SCHED, bool W16>                                     \
     static cudaError_t NAME##_go(const Plan& pl, const Params& p, cudaStream_t st)                \
     {                                                                                             \
-        return run_kernel(reinterpret_cast<const void*>(&rmsq_row_kernel<DT, RES, MODE, VPT, SCHED>), \
-                          pl, p, st);                                                             \
+        return run_kernel(                                                                        \
+            reinterpret_cast<const void*>(&rmsq_row_kernel<DT, RES, MODE, VPT, SCHED, W16>), pl,  \
+            p, st);                                                                               \
+    }                                                                                             \
+    template <int DT, bool RES, int VPT, int SCHED>                                               \
+    static cudaError_t NAME##_w16(const Plan& pl, const Params& p, cudaStream_t st)               \
+    {                                                                                             \
+        if constexpr (DT != DT_F32) {                                                             \
+            if (pl.w16) return NAME##_go<DT, RES, VPT, SCHED, true>(pl, p, st);                   \
+        }                                                                                         \
+        return NAME##_go<DT, RES, VPT, SCHED, false>(pl, p, st);                                  \
     }                                                                                             \
     template <int DT, bool RES, int VPT>                                                          \
     static cudaError_t NAME##_sched(const Plan& pl, const Params& p, cudaStream_t st)             \
     {                                                                                             \
-        return pl.sched == SCHED_PIPE ? NAME##_go<DT, RES, VPT, SCHED_PIPE>(pl, p, st)            \
-                                      : NAME##_go<DT, RES, VPT, SCHED_REG>(pl, p, st);            \
+        return pl.sched == SCHED_PIPE ? NAME##_w16<DT, RES, VPT, SCHED_PIPE>(pl, p, st)           \
+                                      : NAME##_w16<DT, RES, VPT, SCHED_REG>(pl, p, st);           \
     }                                                                                             \
     template <int DT, bool RES>                                                                   \
     static cudaError_t NAME##_vpt(const Plan& pl, const Params& p, cudaStream_t st)               \
