@@ -224,6 +224,8 @@ def run_ours(args):
     from rmsnorm_precision_activation_gb300 import build as B
     B.build()
     import rmsnorm_precision_activation_gb300 as rq
+    if args.no_pdl:
+        rq.rmsq_set_pdl(False)
 
     device = torch.device("cuda", local)
     rows, hidden = STEP_SHAPE
@@ -506,6 +508,8 @@ def main():
     ap.add_argument("--only", default="", help="--report: comma-separated workload names "
                     "(or name:rows:hidden for one MXFP4 sweep point)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-pdl", action="store_true",
+                    help="launch without programmatic dependent launch (for comparison)")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)       # at least 3 untimed warm-up steps, always

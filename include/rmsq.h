@@ -174,6 +174,10 @@ rmsq_status rmsq_device_status(void);
  *                    1, 2, 4 or 8). Returns RMSQ_ERR_VALUE for values out of range; a setting
  *                    that needs more than 512 threads per CTA makes later calls fail with
  *                    RMSQ_ERR_SHAPE.
+ * rmsq_set_pdl      kernels are launched with programmatic dependent launch by default (a
+ *                    launch may be scheduled while the previous kernel on the stream finishes; it
+ *                    waits for that kernel before touching global memory). 0 turns this off for
+ *                    later calls. Returns the previous setting.
  * rmsq_set_wait_timeout_ns  bound of every device-side wait (default 2e9 ns).
  * rmsq_selftest_wait_timeout  launches one CTA that waits on a barrier nothing will complete,
  *                    bounded by timeout_ns, so a test can check that the bound fires and is
@@ -184,6 +188,7 @@ rmsq_status rmsq_device_status(void);
  * ------------------------------------------------------------------------------------------- */
 int rmsq_set_schedule(int schedule);
 rmsq_status rmsq_set_tuning(int stages, int ctas_per_sm, int vectors_per_thread);
+int rmsq_set_pdl(int enable);
 void rmsq_set_wait_timeout_ns(uint64_t timeout_ns);
 rmsq_status rmsq_selftest_wait_timeout(uint64_t timeout_ns, void* stream);
 rmsq_status rmsq_debug_convert(int fmt, const float* in, uint8_t* out, int64_t n, void* stream);

@@ -42,6 +42,7 @@ SIGNATURES = {
     "rmsq_device_status": ([], _I),
     "rmsq_set_schedule": ([_I], _I),
     "rmsq_set_tuning": ([_I, _I, _I], _I),
+    "rmsq_set_pdl": ([_I], _I),
     "rmsq_set_wait_timeout_ns": ([_U64], None),
     "rmsq_selftest_wait_timeout": ([_U64, _P], _I),
     "rmsq_debug_convert": ([_I, _P, _P, _I64, _P], _I),
@@ -228,6 +229,10 @@ def rmsq_set_schedule(schedule: int) -> int:
 
 def rmsq_set_tuning(stages: int = 0, ctas_per_sm: int = 0, vectors_per_thread: int = 0):
     _check(lib().rmsq_set_tuning(stages, ctas_per_sm, vectors_per_thread), "rmsq_set_tuning")
+
+
+def rmsq_set_pdl(enable: bool) -> bool:
+    return bool(lib().rmsq_set_pdl(int(bool(enable))))
 
 
 def rmsq_set_wait_timeout_ns(ns: int):

@@ -20,6 +20,7 @@ static std::atomic<int> g_tune_ctas{0};
 static std::atomic<int> g_tune_vpt{0};
 static std::atomic<unsigned long long> g_timeout_ns{2000000000ull};
 static std::atomic<unsigned long long> g_launches{0};
+static std::atomic<bool> g_pdl{true};
 
 constexpr int kMaxDevices = 64;
 
@@ -88,6 +89,11 @@ cudaError_t run_kernel(const void* fn, const Plan& pl, const Params& p, cudaStre
             cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                  di.smem_optin);
             if (e != cudaSuccess) return e;
+            // The kernels stage rows in shared memory and barely use L1: prefer the largest
+            // shared-memory carveout so the row rings of several CTAs fit on one SM.
+            e = cudaFuncSetAttribute(fn, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                     cudaSharedmemCarveoutMaxShared);
+            if (e != cudaSuccess) return e;
             int b = 0;
             e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, fn, pl.threads, pl.smem);
             if (e != cudaSuccess) return e;
@@ -103,8 +109,19 @@ cudaError_t run_kernel(const void* fn, const Plan& pl, const Params& p, cudaStre
     long long grid = static_cast<long long>(blocks) * di.sms;
     if (grid > p.rows) grid = p.rows;
     void* args[] = {const_cast<Params*>(&p)};
-    cudaError_t e = cudaLaunchKernel(fn, dim3(static_cast<unsigned>(grid)), dim3(pl.threads), args,
-                                     static_cast<size_t>(pl.smem), stream);
+    // Programmatic dependent launch: the kernel may be scheduled while the previous kernel on the
+    // stream finishes; it waits (griddepcontrol.wait) before touching global memory.
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid));
+    cfg.blockDim = dim3(pl.threads);
+    cfg.dynamicSmemBytes = static_cast<size_t>(pl.smem);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = g_pdl.load() ? 1 : 0;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelExC(&cfg, fn, args);
     if (e == cudaSuccess) g_launches.fetch_add(1, std::memory_order_relaxed);
     return e;
 }
@@ -117,10 +134,12 @@ static int elems_per_vec(int dt) { return dt == DT_F32 ? 4 : 8; }
 
 // Pick vectors per thread, CTA size, schedule, ring depth and residency for one call.
 // From on-GPU sweeps (GB300): each thread takes the power of two nearest nv / 128 vectors of 16
-// bytes per row (nv / 256 for FP4 with a residual; FP8 at most 4, so y stays in registers); a
+// bytes per row (nv / 256 for FP4 with a residual; FP8 without W16 at most 4, so y stays in
+// registers); a
 // two-row ring per CTA; FP4 kernels with a residual run best with few CTAs per SM (3), FP4
 // kernels without one and the FP8 kernel with more (8 and 6).
-static bool make_plan(int mode, int dt, bool res, int hidden, const DeviceInfo& di, Plan& pl)
+static bool make_plan(int mode, int dt, bool res, bool w16, int hidden, const DeviceInfo& di,
+                      Plan& pl)
 {
     const int nv = hidden / elems_per_vec(dt);
     pl.mode = mode;
@@ -132,7 +151,7 @@ static bool make_plan(int mode, int dt, bool res, int hidden, const DeviceInfo& 
         const int target = (mode != MODE_FP8 && res) ? 256 : 128;
         vpt = 1;
         while (vpt < 8 && 2 * nv > 3 * target * vpt) vpt *= 2;
-        if (mode == MODE_FP8 && vpt > 4) vpt = 4;
+        if (mode == MODE_FP8 && !w16 && vpt > 4) vpt = 4;
         while (vpt < 8 && (nv + vpt - 1) / vpt > 512) vpt *= 2;
     }
     int threads = ((nv + vpt - 1) / vpt + 31) / 32 * 32;
@@ -214,8 +233,9 @@ static rmsq_status launch(int mode, Params& p, bool res, int dtype, const Device
                           cudaStream_t stream)
 {
     Plan pl;
-    if (!make_plan(mode, dtype, res, p.hidden, di, pl)) return RMSQ_ERR_SHAPE;
-    pl.w16 = dtype != DT_F32 && p.offset == 0.0f;
+    const bool w16 = dtype != DT_F32 && p.offset == 0.0f;
+    if (!make_plan(mode, dtype, res, w16, p.hidden, di, pl)) return RMSQ_ERR_SHAPE;
+    pl.w16 = w16;
     p.stages = pl.stages;
     cudaError_t e;
     switch (mode) {
@@ -443,6 +463,11 @@ extern "C" rmsq_status rmsq_set_tuning(int stages, int ctas_per_sm, int vectors_
     g_tune_ctas = ctas_per_sm;
     g_tune_vpt = vectors_per_thread;
     return RMSQ_OK;
+}
+
+extern "C" int rmsq_set_pdl(int enable)
+{
+    return g_pdl.exchange(enable != 0) ? 1 : 0;
 }
 
 extern "C" void rmsq_set_wait_timeout_ns(uint64_t timeout_ns)

@@ -616,9 +616,9 @@ struct GammaRegs<E, VPT, false> {
     }
 };
 
-// Shared memory after the stage ring: [2][32] float2 sum-of-squares partials, [32] row amax,
-// [128] NVFP4 element factors gs / dec(s) indexed by the E4M3 block-scale code.
-constexpr int kRedFloats = 2 * 32 * 2 + 32 + 128;
+// Shared memory after the stage ring: [2][32] float2 sum-of-squares partials, [2][32] row
+// maxima, [128] NVFP4 element factors gs / dec(s) indexed by the E4M3 block-scale code.
+constexpr int kRedFloats = 2 * 32 * 2 + 2 * 32 + 128;
 
 // ------------------------------------------------------------------------------------------
 // The kernel
@@ -636,7 +636,12 @@ rmsq_row_kernel(const Params p)
     constexpr int BLOCK = MODE == MODE_NVFP4 ? 16 : 32;             // FP4 scale block
     constexpr int GROUP = MODE == MODE_FP8 ? 1 : BLOCK / EPV;        // lanes per FP4 block
     constexpr bool EXACT = MODE == MODE_FP8;
-    constexpr bool KEEP_Y = VPT <= 4;                                // FP8: y held in registers
+    // FP8 with W16: s * w is exact, so max |y| = RN(rstd * max |s w|) and the row max of |s w|
+    // is reduced together with the sum of squares: one CTA barrier per row, y formed once in
+    // the quantisation pass. Otherwise y is formed after rstd, kept in registers (up to four
+    // vectors per thread) and its max reduced at a second barrier.
+    constexpr bool ONE_BAR = MODE == MODE_FP8 && W16;
+    constexpr bool KEEP_Y = VPT <= 4 && !ONE_BAR;
 
     extern __shared__ __align__(128) unsigned char smem[];
 
@@ -652,13 +657,27 @@ rmsq_row_kernel(const Params p)
 
     float* red = reinterpret_cast<float*>(smem + static_cast<size_t>(S) * stage_bytes);
     float2* red_ss_all = reinterpret_cast<float2*>(red);                    // [2][32]
-    float* red_max = red + 128;                                             // [32]
-    float* nv_factor = red + 160;                                           // [128]
+    float* red_max_all = red + 128;                                         // [2][32]
+    float* nv_factor = red + 192;                                           // [128]
     uint64_t* bars = reinterpret_cast<uint64_t*>(red + kRedFloats);         // [S]
 
     const uint4* __restrict__ xg = static_cast<const uint4*>(p.x);
     const uint4* __restrict__ rg = static_cast<const uint4*>(p.res);
     uint4* __restrict__ rog = static_cast<uint4*>(p.res_out);
+
+    uint64_t policy = 0;
+    if constexpr (SCHED == SCHED_PIPE) {
+        policy = l2_evict_first_policy();
+        if (tid == 0) {
+            for (int s = 0; s < S; ++s) mbar_init(smem_u32(&bars[s]), 1);
+            fence_mbar_init();
+        }
+    }
+    // Programmatic dependent launch: everything above touches only shared memory and registers.
+    // Wait here until the previous kernel on the stream has completed and its writes are
+    // visible, then let the next one start its own prologue while this grid runs.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;");
 
     float gs = 1.0f, gs_over_6 = 0.0f;
     if constexpr (MODE == MODE_NVFP4) {
@@ -670,15 +689,8 @@ rmsq_row_kernel(const Params p)
             nv_factor[c] = (c == 0 || c == 0x7F) ? 0.0f : __fdiv_rn(gs, ds);
         }
     }
-
-    uint64_t policy = 0;
+    if constexpr (SCHED == SCHED_PIPE || MODE == MODE_NVFP4) __syncthreads();
     if constexpr (SCHED == SCHED_PIPE) {
-        policy = l2_evict_first_policy();
-        if (tid == 0) {
-            for (int s = 0; s < S; ++s) mbar_init(smem_u32(&bars[s]), 1);
-            fence_mbar_init();
-        }
-        __syncthreads();
         if (tid == 0) {
             for (int s = 0; s < S; ++s) {
                 const long long row = blockIdx.x + static_cast<long long>(s) * gridDim.x;
@@ -690,8 +702,6 @@ rmsq_row_kernel(const Params p)
                 if constexpr (RES) bulk_load(dst + row_bytes, rg + row * nv, row_bytes, bar, policy);
             }
         }
-    } else if constexpr (MODE == MODE_NVFP4) {
-        __syncthreads();
     }
 
     const float2 offset2 = splat(p.offset);
@@ -723,6 +733,7 @@ rmsq_row_kernel(const Params p)
         }
         uint4 s[VPT];
         float2 acc_hi = make_float2(0.0f, 0.0f), acc_lo = make_float2(0.0f, 0.0f);
+        float pmax = 0.0f;      // ONE_BAR: max |s w| over this thread's elements
 #pragma unroll
         for (int k = 0; k < VPT; ++k) {
             const int v = tid + k * T;
@@ -753,6 +764,13 @@ rmsq_row_kernel(const Params p)
                             acc_hi = t;
                             acc_lo = add2(acc_lo, e);
                         }
+                        if constexpr (ONE_BAR) {
+                            const uint32_t gv[4] = {G.g[k].x, G.g[k].y, G.g[k].z, G.g[k].w};
+                            float2 pw[NP];
+#pragma unroll
+                            for (int j = 0; j < NP; ++j) pw[j] = E::mul_halves(sv[j], gv[j]);
+                            pmax = fmaxf(pmax, absmax_pairs(pw));
+                        }
                     } else {
                         // two independent accumulator pairs shorten the dependency chain
                         acc_hi = E::sq_acc(sv[0], acc_hi);
@@ -782,7 +800,12 @@ rmsq_row_kernel(const Params p)
         }
         // ---- CTA reduction of the sum of squares -> rstd ----------------------------------
         float2* red_ss = red_ss_all + rbuf * 32;
+        float* red_max = red_max_all + rbuf * 32;
         rbuf ^= 1;
+        if constexpr (ONE_BAR) {
+            pmax = warp_max(pmax);
+            if (lane == 0) red_max[warp] = pmax;
+        }
         FF ss;
         if constexpr (EXACT) {
             ss = ff_add(FF{acc_hi.x, acc_lo.x}, FF{acc_hi.y, acc_lo.y});
@@ -835,6 +858,13 @@ rmsq_row_kernel(const Params p)
                 t.hi = __shfl_sync(0xFFFFFFFFu, t.hi, 0);
                 t.lo = __shfl_sync(0xFFFFFFFFu, t.lo, 0);
                 rstd = h_pow2 ? rstd_from_sum_pow2(t, inv_h, p.eps) : rstd_from_sum(t, Hf, p.eps);
+                if constexpr (ONE_BAR) {
+                    float m = lane < nwarps ? red_max[lane] : 0.0f;
+#pragma unroll
+                    for (int o = 8; o > 0; o >>= 1)
+                        if (o < red_lanes) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+                    pmax = __shfl_sync(0xFFFFFFFFu, m, 0);
+                }
             } else {
                 float t = part.x;
 #pragma unroll
@@ -877,40 +907,38 @@ rmsq_row_kernel(const Params p)
             // already the correctly rounded product; otherwise the FMA split forms it.
             float2 y[KEEP_Y ? VPT : 1][NP];
             float amax = 0.0f;
-            if constexpr (sw_exact) {
-#pragma unroll
-                for (int k = 0; k < VPT; ++k) {
-                    float2 yy[NP];
-                    sw_pairs(k, yy);
-#pragma unroll
-                    for (int j = 0; j < NP; ++j) {
-                        yy[j] = mul2(yy[j], rstd2);
-                        if constexpr (KEEP_Y) y[k][j] = yy[j];
-                    }
-                    amax = fmaxf(amax, absmax_pairs(yy));
-                }
+            if constexpr (ONE_BAR) {
+                amax = pmax > 0.0f ? __fmul_rn(pmax, rstd) : 0.0f;   // = max |RN(s w rstd)|
             } else {
 #pragma unroll
                 for (int k = 0; k < VPT; ++k) {
-                    float2 f[NP], w[NP], yy[NP];
-                    E::pairs(s[k], f);
-                    G.get(k, w);
+                    float2 yy[NP];
+                    if constexpr (sw_exact) {
+                        sw_pairs(k, yy);
 #pragma unroll
-                    for (int j = 0; j < NP; ++j) {
-                        yy[j] = norm_mul2(f[j], w[j], rstd2);
-                        if constexpr (KEEP_Y) y[k][j] = yy[j];
+                        for (int j = 0; j < NP; ++j) yy[j] = mul2(yy[j], rstd2);
+                    } else {
+                        float2 f[NP], w[NP];
+                        E::pairs(s[k], f);
+                        G.get(k, w);
+#pragma unroll
+                        for (int j = 0; j < NP; ++j) yy[j] = norm_mul2(f[j], w[j], rstd2);
+                    }
+                    if constexpr (KEEP_Y) {
+#pragma unroll
+                        for (int j = 0; j < NP; ++j) y[k][j] = yy[j];
                     }
                     amax = fmaxf(amax, absmax_pairs(yy));
                 }
-            }
-            amax = warp_max(amax);
-            if (lane == 0) red_max[warp] = amax;
-            __syncthreads();
-            amax = lane < nwarps ? red_max[lane] : 0.0f;
+                amax = warp_max(amax);
+                if (lane == 0) red_max[warp] = amax;
+                __syncthreads();
+                amax = lane < nwarps ? red_max[lane] : 0.0f;
 #pragma unroll
-            for (int o = 8; o > 0; o >>= 1)
-                if (o < red_lanes) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
-            amax = __shfl_sync(0xFFFFFFFFu, amax, 0);
+                for (int o = 8; o > 0; o >>= 1)
+                    if (o < red_lanes) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
+                amax = __shfl_sync(0xFFFFFFFFu, amax, 0);
+            }
             float scale = __fdiv_rn(fminf(amax, p.scale_ub), 448.0f);
             if (p.scale_dtype == DT_BF16) {
                 uint16_t h;
