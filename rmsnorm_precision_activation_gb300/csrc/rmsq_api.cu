@@ -134,10 +134,10 @@ static int elems_per_vec(int dt) { return dt == DT_F32 ? 4 : 8; }
 
 // Pick vectors per thread, CTA size, schedule, ring depth and residency for one call.
 // From on-GPU sweeps (GB300): each thread takes the power of two nearest nv / 128 vectors of 16
-// bytes per row (nv / 256 for FP4 with a residual; FP8 without W16 at most 4, so y stays in
-// registers); a
-// two-row ring per CTA; FP4 kernels with a residual run best with few CTAs per SM (3), FP4
-// kernels without one and the FP8 kernel with more (8 and 6).
+// bytes per row (FP8 without W16 at most 4, so y stays in registers), except FP4 with a residual:
+// 2 vectors per thread up to hidden 4096 (bf16) and 8 above; a two-row ring per CTA (three for
+// short FP4 rows); few CTAs per SM for FP4 with a residual (4 / 3 / 2 as rows grow) and the W16
+// FP8 kernel (4), more for FP4 without one (8) and the other FP8 kernels (6).
 static bool make_plan(int mode, int dt, bool res, bool w16, int hidden, const DeviceInfo& di,
                       Plan& pl)
 {
@@ -147,11 +147,16 @@ static bool make_plan(int mode, int dt, bool res, bool w16, int hidden, const De
     pl.res = res;
     int vpt = g_tune_vpt.load();
     if (vpt == 0) {
-        // vectors per thread: the power of two nearest nv / target threads
-        const int target = (mode != MODE_FP8 && res) ? 256 : 128;
-        vpt = 1;
-        while (vpt < 8 && 2 * nv > 3 * target * vpt) vpt *= 2;
-        if (mode == MODE_FP8 && !w16 && vpt > 4) vpt = 4;
+        if (mode != MODE_FP8 && mode != MODE_AMAX && res) {
+            // FP4 with a residual (bandwidth-bound): ~128 threads for short rows, 256 at 4096,
+            // 8 vectors per thread from 5120 on
+            vpt = nv >= 640 ? 8 : (nv >= 512 ? 2 : (nv >= 256 ? 2 : 1));
+        } else {
+            // the power of two nearest nv / 128 vectors per thread
+            vpt = 1;
+            while (vpt < 8 && 2 * nv > 3 * 128 * vpt) vpt *= 2;
+            if (mode == MODE_FP8 && !w16 && vpt > 4) vpt = 4;
+        }
         while (vpt < 8 && (nv + vpt - 1) / vpt > 512) vpt *= 2;
     }
     int threads = ((nv + vpt - 1) / vpt + 31) / 32 * 32;
@@ -166,13 +171,13 @@ static bool make_plan(int mode, int dt, bool res, bool w16, int hidden, const De
     pl.sched = (forced == SCHED_REG || !pipe_fits) ? SCHED_REG : SCHED_PIPE;
     pl.ctas_per_sm = g_tune_ctas.load();
     if (pl.ctas_per_sm == 0) {
-        if (mode == MODE_FP8) pl.ctas_per_sm = 6;
+        if (mode == MODE_FP8) pl.ctas_per_sm = w16 ? 4 : 6;
         else if (!res) pl.ctas_per_sm = 8;
-        else pl.ctas_per_sm = 3;
+        else pl.ctas_per_sm = nv < 512 ? 4 : (nv < 1024 ? 3 : 2);
     }
     if (pl.sched == SCHED_PIPE) {
         int stages = g_tune_stages.load();
-        if (stages == 0) stages = 2;
+        if (stages == 0) stages = (mode != MODE_FP8 && res && nv < 512) ? 3 : 2;
         while (stages > 2 && stages * stage + red_bytes + stages * 8 > di.smem_optin) --stages;
         pl.stages = stages;
         pl.smem = static_cast<int>(stages * stage) + red_bytes + stages * 8;

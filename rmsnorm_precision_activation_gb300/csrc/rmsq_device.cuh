@@ -158,6 +158,13 @@ __device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr)
     return v;
 }
 
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint4 v)
+{
+    asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z),
+                 "r"(v.w)
+                 : "memory");
+}
+
 __device__ __forceinline__ void st_v4(void* p, uint4 v)
 {
     asm volatile("st.global.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z),
@@ -641,7 +648,14 @@ rmsq_row_kernel(const Params p)
     // the quantisation pass. Otherwise y is formed after rstd, kept in registers (up to four
     // vectors per thread) and its max reduced at a second barrier.
     constexpr bool ONE_BAR = MODE == MODE_FP8 && W16;
-    constexpr bool KEEP_Y = VPT <= 4 && !ONE_BAR;
+    // SCHED_PIPE can keep the row in its shared-memory slot until the row is done: pass 1 writes
+    // the residual sum s back over x and later passes re-read it, so no row data is held in
+    // registers across the CTA barrier (the slot is refilled after an end-of-row barrier). That
+    // pays for the bandwidth-bound kernels (MXFP4, the W16 FP8 kernel, the amax pre-pass); the
+    // instruction-bound ones (NVFP4 without residual, FP8 with an offset or fp32 input) keep s in
+    // registers and refill the slot right after the sum-of-squares barrier.
+    constexpr bool SMEM_S = SCHED == SCHED_PIPE && MODE != MODE_NVFP4 && (MODE != MODE_FP8 || W16);
+    constexpr bool KEEP_Y = VPT <= 4 && !ONE_BAR && !SMEM_S;
 
     extern __shared__ __align__(128) unsigned char smem[];
 
@@ -750,6 +764,7 @@ rmsq_row_kernel(const Params p)
                 if constexpr (RES) {
                     s[k] = E::add(xv, rv);
                     if constexpr (MODE != MODE_AMAX) st_v4(rog + row * nv + v, s[k]);
+                    if constexpr (SMEM_S) st_shared_v4(stage_addr + v * 16u, s[k]);
                 } else {
                     s[k] = xv;
                 }
@@ -835,8 +850,9 @@ rmsq_row_kernel(const Params p)
             }
             return;
         }
-        if constexpr (SCHED == SCHED_PIPE) {
-            // Every thread has read this buffer: refill it with the row S iterations ahead.
+        if constexpr (SCHED == SCHED_PIPE && !SMEM_S) {
+            // Every thread has read this slot (s is held in registers): refill it now with the
+            // row S iterations ahead.
             const long long nrow = row + static_cast<long long>(S) * gridDim.x;
             if (tid == 0 && nrow < p.rows) {
                 fence_proxy_async_smem();
@@ -875,16 +891,26 @@ rmsq_row_kernel(const Params p)
             }
         }
         const float2 rstd2 = splat(rstd);
+        // the residual sum s of vector k (zero past the row end)
+        auto get_s = [&](int k) -> uint4 {
+            if constexpr (SMEM_S) {
+                const int v = tid + k * T;
+                return v < nv ? ld_shared_v4(stage_addr + v * 16u) : make_uint4(0, 0, 0, 0);
+            } else {
+                return s[k];
+            }
+        };
         // s * w for the pairs of vector k (exact when W16)
         auto sw_pairs = [&](int k, float2 (&out)[NP]) {
+            const uint4 sk = get_s(k);
             if constexpr (W16) {
-                const uint32_t sv[4] = {s[k].x, s[k].y, s[k].z, s[k].w};
+                const uint32_t sv[4] = {sk.x, sk.y, sk.z, sk.w};
                 const uint32_t gv[4] = {G.g[k].x, G.g[k].y, G.g[k].z, G.g[k].w};
 #pragma unroll
                 for (int j = 0; j < NP; ++j) out[j] = E::mul_halves(sv[j], gv[j]);
             } else {
                 float2 f[NP], w[NP];
-                E::pairs(s[k], f);
+                E::pairs(sk, f);
                 G.get(k, w);
 #pragma unroll
                 for (int j = 0; j < NP; ++j) out[j] = mul2(f[j], w[j]);
@@ -919,7 +945,7 @@ rmsq_row_kernel(const Params p)
                         for (int j = 0; j < NP; ++j) yy[j] = mul2(yy[j], rstd2);
                     } else {
                         float2 f[NP], w[NP];
-                        E::pairs(s[k], f);
+                        E::pairs(get_s(k), f);
                         G.get(k, w);
 #pragma unroll
                         for (int j = 0; j < NP; ++j) yy[j] = norm_mul2(f[j], w[j], rstd2);
@@ -971,7 +997,7 @@ rmsq_row_kernel(const Params p)
                     for (int j = 0; j < NP; ++j) yk[j] = mul2(yk[j], rstd2);
                 } else {
                     float2 f[NP], w[NP];
-                    E::pairs(s[k], f);
+                    E::pairs(get_s(k), f);
                     G.get(k, w);
 #pragma unroll
                     for (int j = 0; j < NP; ++j) yk[j] = norm_mul2(f[j], w[j], rstd2);
@@ -1058,6 +1084,19 @@ rmsq_row_kernel(const Params p)
                     }
                     st_u16(outp + v * 2, static_cast<uint16_t>(zero_block ? 0u : cvt_e2m1x4(q)));
                 }
+            }
+        }
+        if constexpr (SMEM_S) {
+            // Every thread is done with this slot: refill it with the row S iterations ahead.
+            __syncthreads();
+            const long long nrow = row + static_cast<long long>(S) * gridDim.x;
+            if (tid == 0 && nrow < p.rows) {
+                fence_proxy_async_smem();
+                const uint32_t bar = smem_u32(&bars[stage]);
+                mbar_arrive_expect_tx(bar, stage_bytes);
+                bulk_load(stage_addr, xg + nrow * nv, row_bytes, bar, policy);
+                if constexpr (RES)
+                    bulk_load(stage_addr + row_bytes, rg + nrow * nv, row_bytes, bar, policy);
             }
         }
         if constexpr (SCHED == SCHED_PIPE) {
