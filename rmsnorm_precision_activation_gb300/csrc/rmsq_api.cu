@@ -158,6 +158,9 @@ static bool make_plan(int mode, int dt, bool res, bool w16, int hidden, const De
             if (mode == MODE_FP8 && !w16 && vpt > 4) vpt = 4;
         }
         while (vpt < 8 && (nv + vpt - 1) / vpt > 512) vpt *= 2;
+        // NVFP4 threads own whole 16-element scale blocks (2 vectors, 4 for fp32 input)
+        const int group = 16 / elems_per_vec(dt);
+        if (mode == MODE_NVFP4 && vpt < group) vpt = group;
     }
     int threads = ((nv + vpt - 1) / vpt + 31) / 32 * 32;
     if (threads > 512) return false;

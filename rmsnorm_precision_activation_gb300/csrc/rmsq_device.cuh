@@ -582,11 +582,13 @@ template <class E, int VPT>
 struct GammaRegs<E, VPT, true> {
     static constexpr int NP = E::EPV / 2;
     float2 w[VPT][NP];
-    __device__ __forceinline__ void load(const uint4* gp, int tid, int T, int nv, float2 off)
+    // group > 1: blocked order, slot k holds vector group * (tid + (k / group) * T) + k % group
+    __device__ __forceinline__ void load(const uint4* gp, int tid, int T, int nv, float2 off,
+                                         int group = 1)
     {
 #pragma unroll
         for (int k = 0; k < VPT; ++k) {
-            const int v = tid + k * T;
+            const int v = group == 1 ? tid + k * T : group * (tid + (k / group) * T) + k % group;
             const uint4 gv = v < nv ? __ldg(gp + v) : make_uint4(0, 0, 0, 0);
             float2 f[NP];
             E::pairs(gv, f);
@@ -606,12 +608,13 @@ struct GammaRegs<E, VPT, false> {
     static constexpr int NP = E::EPV / 2;
     uint4 g[VPT];
     float2 off;
-    __device__ __forceinline__ void load(const uint4* gp, int tid, int T, int nv, float2 o)
+    __device__ __forceinline__ void load(const uint4* gp, int tid, int T, int nv, float2 o,
+                                         int group = 1)
     {
         off = o;
 #pragma unroll
         for (int k = 0; k < VPT; ++k) {
-            const int v = tid + k * T;
+            const int v = group == 1 ? tid + k * T : group * (tid + (k / group) * T) + k % group;
             g[k] = v < nv ? __ldg(gp + v) : make_uint4(0, 0, 0, 0);
         }
     }
@@ -651,10 +654,13 @@ rmsq_row_kernel(const Params p)
     // SCHED_PIPE can keep the row in its shared-memory slot until the row is done: pass 1 writes
     // the residual sum s back over x and later passes re-read it, so no row data is held in
     // registers across the CTA barrier (the slot is refilled after an end-of-row barrier). That
-    // pays for the bandwidth-bound kernels (MXFP4, the W16 FP8 kernel, the amax pre-pass); the
-    // instruction-bound ones (NVFP4 without residual, FP8 with an offset or fp32 input) keep s in
-    // registers and refill the slot right after the sum-of-squares barrier.
-    constexpr bool SMEM_S = SCHED == SCHED_PIPE && MODE != MODE_NVFP4 && (MODE != MODE_FP8 || W16);
+    // pays except for the FP8 kernels with an offset or fp32 input (instruction-bound: they keep s
+    // and y in registers and refill the slot right after the sum-of-squares barrier).
+    constexpr bool SMEM_S = SCHED == SCHED_PIPE && (MODE != MODE_FP8 || W16);
+    // NVFP4 in SCHED_PIPE: pass 2 is blocked, each thread owns whole 16-element scale blocks
+    // (GROUP consecutive vectors, re-read from the slot), so the block scale, its table lookup
+    // and its store happen once per block and the codes leave in one 8-byte store.
+    constexpr bool NV_BLOCKED = MODE == MODE_NVFP4 && SCHED == SCHED_PIPE && VPT >= GROUP;
     constexpr bool KEEP_Y = VPT <= 4 && !ONE_BAR && !SMEM_S;
 
     extern __shared__ __align__(128) unsigned char smem[];
@@ -720,7 +726,7 @@ rmsq_row_kernel(const Params p)
 
     const float2 offset2 = splat(p.offset);
     GammaRegs<E, VPT, !W16 && VPT <= 4> G;
-    G.load(static_cast<const uint4*>(p.gamma), tid, T, nv, offset2);
+    G.load(static_cast<const uint4*>(p.gamma), tid, T, nv, offset2, NV_BLOCKED ? GROUP : 1);
     constexpr bool sw_exact = W16;                            // s * gamma exact in fp32
     const float Hf = static_cast<float>(p.hidden);
     // lanes in the second reduction stage: the smallest power of two >= nwarps
@@ -1023,6 +1029,74 @@ rmsq_row_kernel(const Params p)
                     st_v2(outp + v * 8, c[0] | (c[1] << 16), c[2] | (c[3] << 16));
                 } else {
                     st_u32(outp + v * 4, c[0] | (c[1] << 16));
+                }
+            }
+        } else if constexpr (NV_BLOCKED) {
+            // ---- NVFP4, blocked: thread owns blocks b = tid + kb * T (GROUP vectors each) ---------
+            unsigned char* outp = static_cast<unsigned char*>(p.out) + row * (p.hidden / 2);
+            unsigned char* sp_row = static_cast<unsigned char*>(p.scale_out) +
+                (p.swizzled ? (row >> 7) * (static_cast<long long>(p.k_tiles) * 512) +
+                                  (row & 31) * 16 + ((row & 127) >> 5) * 4
+                            : row * p.nsf);
+            const int nb = nv / GROUP;
+#pragma unroll
+            for (int kb = 0; kb < VPT / GROUP; ++kb) {
+                const int b = tid + kb * T;
+                if (b >= nb) continue;
+                float2 sw[GROUP][NP];
+                float m = 0.0f;
+#pragma unroll
+                for (int j = 0; j < GROUP; ++j) {
+                    const uint4 sk = ld_shared_v4(stage_addr + (b * GROUP + j) * 16u);
+                    const int k = kb * GROUP + j;
+                    if constexpr (W16) {
+                        const uint32_t sv[4] = {sk.x, sk.y, sk.z, sk.w};
+                        const uint32_t gv[4] = {G.g[k].x, G.g[k].y, G.g[k].z, G.g[k].w};
+#pragma unroll
+                        for (int i = 0; i < NP; ++i) sw[j][i] = E::mul_halves(sv[i], gv[i]);
+                    } else {
+                        float2 f[NP], w[NP];
+                        E::pairs(sk, f);
+                        G.get(k, w);
+#pragma unroll
+                        for (int i = 0; i < NP; ++i) sw[j][i] = mul2(f[i], w[i]);
+                    }
+                    m = fmaxf(m, absmax_pairs(sw[j]));
+                }
+                const float a = m > 0.0f ? __fmul_rn(m, rstd) : 0.0f;      // block max |y|
+                const float t = fminf(__fmul_rn(a, gs_over_6), 448.0f);
+                const uint32_t code = cvt_e4m3x2(t, 0.0f) & 0xFFu;
+                const float factor = nv_factor[code & 0x7Fu];
+                sp_row[p.swizzled ? (b >> 2) * 512 + (b & 3) : b] = static_cast<unsigned char>(code);
+                const bool zero_block = !(factor > 0.0f);
+                const float2 f2 = splat(zero_block ? 0.0f : __fmul_rn(factor, rstd));
+                uint32_t packed[GROUP];
+#pragma unroll
+                for (int j = 0; j < GROUP; ++j) {
+                    if constexpr (EPV == 8) {
+                        float q[8];
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            const float2 qq = mul2(sw[j][i], f2);
+                            q[2 * i] = qq.x;
+                            q[2 * i + 1] = qq.y;
+                        }
+                        packed[j] = zero_block ? 0u : cvt_e2m1x8(q);
+                    } else {
+                        float q[4];
+#pragma unroll
+                        for (int i = 0; i < 2; ++i) {
+                            const float2 qq = mul2(sw[j][i], f2);
+                            q[2 * i] = qq.x;
+                            q[2 * i + 1] = qq.y;
+                        }
+                        packed[j] = zero_block ? 0u : cvt_e2m1x4(q);
+                    }
+                }
+                if constexpr (EPV == 8) {
+                    st_v2(outp + b * 8, packed[0], packed[1]);
+                } else {
+                    st_v2(outp + b * 8, packed[0] | (packed[1] << 16), packed[2] | (packed[3] << 16));
                 }
             }
         } else {
