@@ -26,6 +26,7 @@ import argparse
 import hashlib
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -497,6 +498,64 @@ def run_report(args):
         del outs, d
 
 
+# ------------------------------------------------------------------------------------------
+# ncu-backed per-workload table
+# ------------------------------------------------------------------------------------------
+
+NCU_UNITS = {"byte": 1.0, "Kbyte": 1e3, "Mbyte": 1e6, "Gbyte": 1e9, "ns": 1e-9, "nsecond": 1e-9, "us": 1e-6,
+             "usecond": 1e-6, "msecond": 1e-3, "second": 1.0, "%": 1.0}
+
+
+def ncu_table(args):
+    """Markdown table of DRAM figures per workload from the ncu CSV of a `--report` run.
+
+    The CSV is ncu's long format (one row per metric per launch) of `bench.py --report` with the
+    same --only / --report-reps, captured with `-k regex:rmsq_row_kernel`. Launches are assigned
+    to workloads in the order the report runs them: per workload one launch that allocates the
+    outputs, three warm-ups and --report-reps timed ones (NVFP4's global-scale pre-pass,
+    template mode 3, is dropped). The figures are the medians over the timed launches."""
+    import csv
+    with open(args.ncu_table) as f:
+        rows = [ln for ln in f if ln.startswith('"')]
+    launches = {}
+    for r in csv.DictReader(rows):
+        e = launches.setdefault(int(r["ID"]), {"name": r["Kernel Name"]})
+        v = float(r["Metric Value"].replace(",", ""))
+        e[r["Metric Name"]] = v * NCU_UNITS.get(r["Metric Unit"], 1.0)
+    seq = []
+    for _, e in sorted(launches.items()):
+        targs = re.search(r"<([^>]*)>", e["name"]).group(1).split(",")
+        e["mode"] = int(targs[2])
+        if e["mode"] != 3:
+            seq.append(e)
+    only = set(args.only.split(",")) if args.only else None
+    per = 4 + args.report_reps
+    mode_id = {"fp8": 0, "nvfp4": 1, "mxfp4": 2}
+    print("| workload | rows x hidden | ncu duration (us) | DRAM read + write (MB) | algorithmic "
+          "MB | DRAM throughput (% of peak) | algorithmic GB/s at ncu duration |")
+    print("|---|---|---|---|---|---|---|")
+    k = 0
+    for name, rws, hid in report_workloads():
+        if only and name not in only and "%s:%s:%s" % (name, rws, hid) not in only:
+            continue
+        w = W.config(name, rows=rws, hidden=hid)
+        chunk = seq[k:k + per]
+        k += per
+        if len(chunk) < per or any(e["mode"] != mode_id[w.mode] for e in chunk):
+            raise SystemExit("ncu CSV does not match the report's launch sequence at %s" % name)
+        timed = chunk[4:]
+        med = lambda m: statistics.median(e[m] for e in timed)
+        dur = med("gpu__time_duration.sum")
+        traffic = med("dram__bytes_read.sum") + med("dram__bytes_write.sum")
+        pct = med("dram__throughput.avg.pct_of_peak_sustained_elapsed")
+        algo = w.algorithmic_bytes()
+        print("| %s | %d x %d | %.1f | %.1f | %.1f | %.1f | %.0f |"
+              % (name, w.rows, w.hidden, dur * 1e6, traffic / 1e6, algo / 1e6, pct,
+                 algo / dur / 1e9))
+    if k != len(seq):
+        raise SystemExit("ncu CSV has %d launches left over" % (len(seq) - k))
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -511,9 +570,14 @@ def main():
     ap.add_argument("--no-pdl", action="store_true",
                     help="launch without programmatic dependent launch (for comparison)")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--ncu-table", default="", metavar="CSV",
+                    help="print the per-workload DRAM table from the ncu CSV of a --report run "
+                         "(same --only / --report-reps); needs no GPU")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)       # at least 3 untimed warm-up steps, always
-    if args.impl == "reference":
+    if args.ncu_table:
+        ncu_table(args)
+    elif args.impl == "reference":
         run_reference(args)
     elif args.report:
         run_report(args)
