@@ -166,14 +166,18 @@ rmsq_status rmsq_device_status(void);
  * Tuning and diagnostics. None of these is needed for normal use.
  *
  * rmsq_set_schedule  forces the kernel schedule of later calls in this process: 0 = automatic,
- *                    1 = bulk-copy pipeline (rows staged in shared memory by the TMA engine),
- *                    2 = register-staged rows. Returns the previous value. A forced pipeline
- *                    schedule that cannot hold two rows in shared memory falls back to 2.
+ *                    1 = bulk-copy pipeline (rows staged in shared memory by the TMA engine, a
+ *                    CTA per row), 2 = register-staged rows, 3 = row per warp (each warp owns
+ *                    whole rows with its own bulk-copy ring; rows up to 256 vectors of 16 bytes,
+ *                    i.e. hidden <= 2048 for 16-bit input). Returns the previous value. A forced
+ *                    schedule that does not fit the row falls back to 1, and 1 to 2.
  * rmsq_set_tuning    overrides the pipeline depth (stages, 0 = automatic), CTAs per SM
  *                    (0 = automatic) and vectors of 16 bytes per thread per row (0 = automatic;
  *                    1, 2, 4 or 8). Returns RMSQ_ERR_VALUE for values out of range; a setting
  *                    that needs more than 512 threads per CTA makes later calls fail with
  *                    RMSQ_ERR_SHAPE.
+ * rmsq_set_row_warps  warps per CTA of the row-per-warp schedule (0 = automatic, at most 16).
+ *                    Returns RMSQ_ERR_VALUE out of range.
  * rmsq_set_pdl      kernels are launched with programmatic dependent launch by default (a
  *                    launch may be scheduled while the previous kernel on the stream finishes; it
  *                    waits for that kernel before touching global memory). 0 turns this off for
@@ -188,6 +192,7 @@ rmsq_status rmsq_device_status(void);
  * ------------------------------------------------------------------------------------------- */
 int rmsq_set_schedule(int schedule);
 rmsq_status rmsq_set_tuning(int stages, int ctas_per_sm, int vectors_per_thread);
+rmsq_status rmsq_set_row_warps(int warps_per_cta);
 int rmsq_set_pdl(int enable);
 void rmsq_set_wait_timeout_ns(uint64_t timeout_ns);
 rmsq_status rmsq_selftest_wait_timeout(uint64_t timeout_ns, void* stream);

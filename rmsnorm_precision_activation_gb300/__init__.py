@@ -22,7 +22,7 @@ LIB_PATH = os.path.join(_HERE, "librmsq.so")
 
 RMSQ_BF16, RMSQ_FP16, RMSQ_F32 = 0, 1, 2
 SCALE_ROW_MAJOR, SCALE_SWIZZLED_128x4 = 0, 1
-SCHED_AUTO, SCHED_PIPE, SCHED_REG = 0, 1, 2
+SCHED_AUTO, SCHED_PIPE, SCHED_REG, SCHED_WARP = 0, 1, 2, 3
 MAX_HIDDEN = 32768
 
 STATUS = {0: "RMSQ_OK", 1: "RMSQ_ERR_NULL", 2: "RMSQ_ERR_SHAPE", 3: "RMSQ_ERR_ALIGN",
@@ -42,6 +42,7 @@ SIGNATURES = {
     "rmsq_device_status": ([], _I),
     "rmsq_set_schedule": ([_I], _I),
     "rmsq_set_tuning": ([_I, _I, _I], _I),
+    "rmsq_set_row_warps": ([_I], _I),
     "rmsq_set_pdl": ([_I], _I),
     "rmsq_set_wait_timeout_ns": ([_U64], None),
     "rmsq_selftest_wait_timeout": ([_U64, _P], _I),
@@ -229,6 +230,10 @@ def rmsq_set_schedule(schedule: int) -> int:
 
 def rmsq_set_tuning(stages: int = 0, ctas_per_sm: int = 0, vectors_per_thread: int = 0):
     _check(lib().rmsq_set_tuning(stages, ctas_per_sm, vectors_per_thread), "rmsq_set_tuning")
+
+
+def rmsq_set_row_warps(warps_per_cta: int = 0):
+    _check(lib().rmsq_set_row_warps(int(warps_per_cta)), "rmsq_set_row_warps")
 
 
 def rmsq_set_pdl(enable: bool) -> bool:

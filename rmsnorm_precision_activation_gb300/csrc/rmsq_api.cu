@@ -18,6 +18,7 @@ static std::atomic<int> g_schedule{0};
 static std::atomic<int> g_tune_stages{0};
 static std::atomic<int> g_tune_ctas{0};
 static std::atomic<int> g_tune_vpt{0};
+static std::atomic<int> g_tune_warps{0};
 static std::atomic<unsigned long long> g_timeout_ns{2000000000ull};
 static std::atomic<unsigned long long> g_launches{0};
 static std::atomic<bool> g_pdl{true};
@@ -107,7 +108,9 @@ cudaError_t run_kernel(const void* fn, const Plan& pl, const Params& p, cudaStre
     if (blocks < 1) return cudaErrorInvalidConfiguration;
     if (pl.ctas_per_sm > 0 && blocks > pl.ctas_per_sm) blocks = pl.ctas_per_sm;
     long long grid = static_cast<long long>(blocks) * di.sms;
-    if (grid > p.rows) grid = p.rows;
+    const long long rows_per_cta = pl.sched == SCHED_WARP ? pl.threads / 32 : 1;
+    if (grid > (p.rows + rows_per_cta - 1) / rows_per_cta)
+        grid = (p.rows + rows_per_cta - 1) / rows_per_cta;
     void* args[] = {const_cast<Params*>(&p)};
     // Programmatic dependent launch: the kernel may be scheduled while the previous kernel on the
     // stream finishes; it waits (griddepcontrol.wait) before touching global memory.
@@ -145,6 +148,36 @@ static bool make_plan(int mode, int dt, bool res, bool w16, int hidden, const De
     pl.mode = mode;
     pl.dt = dt;
     pl.res = res;
+    const int forced = g_schedule.load();
+    const long long stage = static_cast<long long>(nv) * 16 * (res ? 2 : 1);
+    const int group = 16 / elems_per_vec(dt);
+
+    // Row per warp: a warp holds the row in at most 8 vectors per lane (hidden <= 2048 for
+    // 16-bit input) and each warp keeps its own two-row ring.
+    const int warp_red = kRedFloatsWarp * 4;
+    const bool warp_fits = nv <= 256 && 2 * stage + warp_red + 16 <= di.smem_optin;
+    if (warp_fits && forced == SCHED_WARP) {
+        int vpt = 1;
+        while (32 * vpt < nv) vpt *= 2;
+        if (mode == MODE_NVFP4 && vpt < group) vpt = group;
+        const int tv = g_tune_vpt.load();
+        if (tv > vpt) vpt = tv;
+        int warps = g_tune_warps.load();
+        if (warps == 0) warps = stage <= 2048 ? 4 : (stage <= 4096 ? 2 : 1);
+        int stages = g_tune_stages.load();
+        if (stages == 0) stages = 2;
+        auto bytes = [&](int w, int st) { return w * st * stage + warp_red + w * st * 8; };
+        while (stages > 2 && bytes(warps, stages) > di.smem_optin) --stages;
+        while (warps > 1 && bytes(warps, stages) > di.smem_optin) warps /= 2;
+        pl.sched = SCHED_WARP;
+        pl.vpt = vpt;
+        pl.threads = 32 * warps;
+        pl.stages = stages;
+        pl.smem = static_cast<int>(bytes(warps, stages));
+        pl.ctas_per_sm = g_tune_ctas.load();
+        return true;
+    }
+
     int vpt = g_tune_vpt.load();
     if (vpt == 0) {
         if (mode != MODE_FP8 && mode != MODE_AMAX && res) {
@@ -159,7 +192,6 @@ static bool make_plan(int mode, int dt, bool res, bool w16, int hidden, const De
         }
         while (vpt < 8 && (nv + vpt - 1) / vpt > 512) vpt *= 2;
         // NVFP4 threads own whole 16-element scale blocks (2 vectors, 4 for fp32 input)
-        const int group = 16 / elems_per_vec(dt);
         if (mode == MODE_NVFP4 && vpt < group) vpt = group;
     }
     int threads = ((nv + vpt - 1) / vpt + 31) / 32 * 32;
@@ -168,8 +200,6 @@ static bool make_plan(int mode, int dt, bool res, bool w16, int hidden, const De
     pl.threads = threads;
 
     const int red_bytes = kRedFloats * 4;
-    const long long stage = static_cast<long long>(nv) * 16 * (res ? 2 : 1);
-    const int forced = g_schedule.load();
     const bool pipe_fits = 2 * stage + red_bytes + 2 * 8 <= di.smem_optin;
     pl.sched = (forced == SCHED_REG || !pipe_fits) ? SCHED_REG : SCHED_PIPE;
     pl.ctas_per_sm = g_tune_ctas.load();
@@ -457,7 +487,7 @@ extern "C" rmsq_status rmsq_device_status(void)
 
 extern "C" int rmsq_set_schedule(int schedule)
 {
-    if (schedule < 0 || schedule > 2) schedule = 0;
+    if (schedule < 0 || schedule > 3) schedule = 0;
     return g_schedule.exchange(schedule);
 }
 
@@ -470,6 +500,13 @@ extern "C" rmsq_status rmsq_set_tuning(int stages, int ctas_per_sm, int vectors_
     g_tune_stages = stages;
     g_tune_ctas = ctas_per_sm;
     g_tune_vpt = vectors_per_thread;
+    return RMSQ_OK;
+}
+
+extern "C" rmsq_status rmsq_set_row_warps(int warps_per_cta)
+{
+    if (warps_per_cta < 0 || warps_per_cta > 16) return RMSQ_ERR_VALUE;
+    g_tune_warps = warps_per_cta;
     return RMSQ_OK;
 }
 

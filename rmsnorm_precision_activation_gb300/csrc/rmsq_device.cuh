@@ -6,13 +6,16 @@
 // touches 512 contiguous bytes per step), add the residual, reduce the sum of squares over the
 // CTA, form y = s * rstd * (gamma + offset) and quantise. The row is read from HBM exactly once.
 //
-// Two schedules fetch the row:
+// Three schedules fetch the row:
 //   SCHED_PIPE  persistent CTAs with a ring of `stages` shared-memory row buffers filled by the
 //               TMA bulk-copy engine (cp.async.bulk + mbarrier transaction counts). Thread 0
 //               refills a buffer with the row `stages` iterations ahead as soon as the CTA has
 //               read it, so several rows per SM stay in flight while the CTA computes.
 //   SCHED_REG   persistent CTAs that load their row straight into registers with 128-bit
 //               streaming loads; latency is hidden by the other CTAs on the SM.
+//   SCHED_WARP  row per warp, for short rows: every warp of a CTA owns whole rows with its own
+//               ring of row buffers and mbarriers (lane 0 issues the bulk copies), and all
+//               reductions are warp shuffles -- no CTA barrier and no cross-warp stage per row.
 //
 // Method sources: Modular Mojo API docs "rms_norm_fused_fp8" / "allreduce_residual_rmsnorm_fp8"
 // (FP8 row scale with scale_ub, residual_output, weight_offset on gamma) and FlashInfer
@@ -28,7 +31,7 @@ namespace rmsq {
 enum { DT_BF16 = 0, DT_FP16 = 1, DT_F32 = 2 };
 // MODE_AMAX is the NVFP4 global-scale pre-pass: y is formed but only max |y| leaves the kernel.
 enum { MODE_FP8 = 0, MODE_NVFP4 = 1, MODE_MXFP4 = 2, MODE_AMAX = 3 };
-enum { SCHED_PIPE = 1, SCHED_REG = 2 };
+enum { SCHED_PIPE = 1, SCHED_REG = 2, SCHED_WARP = 3 };
 
 // Error flag bits set on the device.
 enum { ERRF_WAIT_TIMEOUT = 1u };
@@ -52,7 +55,7 @@ struct Params {
     int swizzled;             // FP4: swizzled 128x4 scale layout
     int nsf;                  // FP4: block scales per row
     int k_tiles;              // FP4 swizzled: 4-scale tiles per row
-    int stages;               // SCHED_PIPE: ring depth
+    int stages;               // SCHED_PIPE / SCHED_WARP: ring depth (per ring)
     unsigned long long timeout_ns;
 };
 
@@ -626,9 +629,11 @@ struct GammaRegs<E, VPT, false> {
     }
 };
 
-// Shared memory after the stage ring: [2][32] float2 sum-of-squares partials, [2][32] row
-// maxima, [128] NVFP4 element factors gs / dec(s) indexed by the E4M3 block-scale code.
+// Shared memory after the stage rings: [2][32] float2 sum-of-squares partials, [2][32] row
+// maxima, [128] NVFP4 element factors gs / dec(s) indexed by the E4M3 block-scale code. The
+// row-per-warp schedule reduces in registers and keeps only the factor table.
 constexpr int kRedFloats = 2 * 32 * 2 + 2 * 32 + 128;
+constexpr int kRedFloatsWarp = 128;
 
 // ------------------------------------------------------------------------------------------
 // The kernel
@@ -651,16 +656,20 @@ rmsq_row_kernel(const Params p)
     // the quantisation pass. Otherwise y is formed after rstd, kept in registers (up to four
     // vectors per thread) and its max reduced at a second barrier.
     constexpr bool ONE_BAR = MODE == MODE_FP8 && W16;
-    // SCHED_PIPE can keep the row in its shared-memory slot until the row is done: pass 1 writes
+    // SCHED_WARP: every warp is its own row processor (rows, ring and mbarriers per warp); the
+    // bulk-copy ring logic is shared with SCHED_PIPE.
+    constexpr bool WARP_ROWS = SCHED == SCHED_WARP;
+    constexpr bool RING = SCHED == SCHED_PIPE || WARP_ROWS;
+    // The ring schedules can keep the row in its shared-memory slot until the row is done: pass 1 writes
     // the residual sum s back over x and later passes re-read it, so no row data is held in
     // registers across the CTA barrier (the slot is refilled after an end-of-row barrier). That
     // pays except for the FP8 kernels with an offset or fp32 input (instruction-bound: they keep s
     // and y in registers and refill the slot right after the sum-of-squares barrier).
-    constexpr bool SMEM_S = SCHED == SCHED_PIPE && (MODE != MODE_FP8 || W16);
-    // NVFP4 in SCHED_PIPE: pass 2 is blocked, each thread owns whole 16-element scale blocks
+    constexpr bool SMEM_S = RING && (MODE != MODE_FP8 || W16);
+    // NVFP4 with a ring: pass 2 is blocked, each thread owns whole 16-element scale blocks
     // (GROUP consecutive vectors, re-read from the slot), so the block scale, its table lookup
     // and its store happen once per block and the codes leave in one 8-byte store.
-    constexpr bool NV_BLOCKED = MODE == MODE_NVFP4 && SCHED == SCHED_PIPE && VPT >= GROUP;
+    constexpr bool NV_BLOCKED = MODE == MODE_NVFP4 && RING && VPT >= GROUP;
     constexpr bool KEEP_Y = VPT <= 4 && !ONE_BAR && !SMEM_S;
 
     extern __shared__ __align__(128) unsigned char smem[];
@@ -670,26 +679,38 @@ rmsq_row_kernel(const Params p)
     const int lane = tid & 31;
     const int warp = tid >> 5;
     const int nwarps = T >> 5;
+    const int rt = WARP_ROWS ? lane : tid;       // this thread's index within its row
+    const int RT = WARP_ROWS ? 32 : T;           // threads per row
     const int nv = p.nvec;
     const uint32_t row_bytes = static_cast<uint32_t>(nv) * 16u;
     const uint32_t stage_bytes = row_bytes * (RES ? 2u : 1u);
-    const int S = SCHED == SCHED_PIPE ? p.stages : 0;
+    const int S = RING ? p.stages : 0;
+    const int nrings = WARP_ROWS ? nwarps : 1;
 
-    float* red = reinterpret_cast<float*>(smem + static_cast<size_t>(S) * stage_bytes);
+    float* red = reinterpret_cast<float*>(smem + static_cast<size_t>(S) * nrings * stage_bytes);
     float2* red_ss_all = reinterpret_cast<float2*>(red);                    // [2][32]
     float* red_max_all = red + 128;                                         // [2][32]
-    float* nv_factor = red + 192;                                           // [128]
-    uint64_t* bars = reinterpret_cast<uint64_t*>(red + kRedFloats);         // [S]
+    float* nv_factor = WARP_ROWS ? red : red + 192;                         // [128]
+    uint64_t* bars_all =
+        reinterpret_cast<uint64_t*>(red + (WARP_ROWS ? kRedFloatsWarp : kRedFloats));  // [nrings][S]
+    // this thread's ring: its slots, its mbarriers, the thread that refills it, and its rows
+    unsigned char* ring = smem + (WARP_ROWS ? static_cast<size_t>(warp) * S * stage_bytes : 0);
+    uint64_t* bars = bars_all + (WARP_ROWS ? warp * S : 0);
+    const bool issuer = WARP_ROWS ? lane == 0 : tid == 0;
+    const long long row0 = WARP_ROWS ? static_cast<long long>(blockIdx.x) * nwarps + warp
+                                     : static_cast<long long>(blockIdx.x);
+    const long long rstep = WARP_ROWS ? static_cast<long long>(gridDim.x) * nwarps
+                                      : static_cast<long long>(gridDim.x);
 
     const uint4* __restrict__ xg = static_cast<const uint4*>(p.x);
     const uint4* __restrict__ rg = static_cast<const uint4*>(p.res);
     uint4* __restrict__ rog = static_cast<uint4*>(p.res_out);
 
     uint64_t policy = 0;
-    if constexpr (SCHED == SCHED_PIPE) {
+    if constexpr (RING) {
         policy = l2_evict_first_policy();
         if (tid == 0) {
-            for (int s = 0; s < S; ++s) mbar_init(smem_u32(&bars[s]), 1);
+            for (int s = 0; s < S * nrings; ++s) mbar_init(smem_u32(&bars_all[s]), 1);
             fence_mbar_init();
         }
     }
@@ -709,14 +730,14 @@ rmsq_row_kernel(const Params p)
             nv_factor[c] = (c == 0 || c == 0x7F) ? 0.0f : __fdiv_rn(gs, ds);
         }
     }
-    if constexpr (SCHED == SCHED_PIPE || MODE == MODE_NVFP4) __syncthreads();
-    if constexpr (SCHED == SCHED_PIPE) {
-        if (tid == 0) {
+    if constexpr (RING || MODE == MODE_NVFP4) __syncthreads();
+    if constexpr (RING) {
+        if (issuer) {
             for (int s = 0; s < S; ++s) {
-                const long long row = blockIdx.x + static_cast<long long>(s) * gridDim.x;
+                const long long row = row0 + static_cast<long long>(s) * rstep;
                 if (row >= p.rows) break;
                 const uint32_t bar = smem_u32(&bars[s]);
-                const uint32_t dst = smem_u32(smem + static_cast<size_t>(s) * stage_bytes);
+                const uint32_t dst = smem_u32(ring + static_cast<size_t>(s) * stage_bytes);
                 mbar_arrive_expect_tx(bar, stage_bytes);
                 bulk_load(dst, xg + row * nv, row_bytes, bar, policy);
                 if constexpr (RES) bulk_load(dst + row_bytes, rg + row * nv, row_bytes, bar, policy);
@@ -726,7 +747,7 @@ rmsq_row_kernel(const Params p)
 
     const float2 offset2 = splat(p.offset);
     GammaRegs<E, VPT, !W16 && VPT <= 4> G;
-    G.load(static_cast<const uint4*>(p.gamma), tid, T, nv, offset2, NV_BLOCKED ? GROUP : 1);
+    G.load(static_cast<const uint4*>(p.gamma), rt, RT, nv, offset2, NV_BLOCKED ? GROUP : 1);
     constexpr bool sw_exact = W16;                            // s * gamma exact in fp32
     const float Hf = static_cast<float>(p.hidden);
     // lanes in the second reduction stage: the smallest power of two >= nwarps
@@ -741,14 +762,14 @@ rmsq_row_kernel(const Params p)
     int stage = 0;          // ring slot of this row, and the mbarrier phase parity to wait for
     uint32_t parity = 0;
     int rbuf = 0;           // which of the two sum-of-squares reduction buffers this row uses
-    for (long long row = blockIdx.x; row < p.rows; row += gridDim.x) {
+    for (long long row = row0; row < p.rows; row += rstep) {
         const uint4* __restrict__ xrow = xg + row * nv;
         const uint4* __restrict__ rrow = RES ? rg + row * nv : nullptr;
         // ---- load the row, add the residual, write residual_output, sum of squares ----------
         bool timed_out = false;
         uint32_t stage_addr = 0;
-        if constexpr (SCHED == SCHED_PIPE) {
-            stage_addr = smem_u32(smem + static_cast<size_t>(stage) * stage_bytes);
+        if constexpr (RING) {
+            stage_addr = smem_u32(ring + static_cast<size_t>(stage) * stage_bytes);
             timed_out = !mbar_wait_bounded(smem_u32(&bars[stage]), parity, p.timeout_ns);
         }
         uint4 s[VPT];
@@ -756,11 +777,11 @@ rmsq_row_kernel(const Params p)
         float pmax = 0.0f;      // ONE_BAR: max |s w| over this thread's elements
 #pragma unroll
         for (int k = 0; k < VPT; ++k) {
-            const int v = tid + k * T;
+            const int v = rt + k * RT;
             s[k] = make_uint4(0, 0, 0, 0);
             if (v < nv && !timed_out) {
                 uint4 xv, rv;
-                if constexpr (SCHED == SCHED_PIPE) {
+                if constexpr (RING) {
                     xv = ld_shared_v4(stage_addr + v * 16u);
                     if constexpr (RES) rv = ld_shared_v4(stage_addr + row_bytes + v * 16u);
                 } else {
@@ -825,7 +846,7 @@ rmsq_row_kernel(const Params p)
         rbuf ^= 1;
         if constexpr (ONE_BAR) {
             pmax = warp_max(pmax);
-            if (lane == 0) red_max[warp] = pmax;
+            if (!WARP_ROWS && lane == 0) red_max[warp] = pmax;
         }
         FF ss;
         if constexpr (EXACT) {
@@ -835,16 +856,19 @@ rmsq_row_kernel(const Params p)
         } else {
             ss = FF{warp_sum(__fadd_rn(__fadd_rn(acc_hi.x, acc_hi.y), __fadd_rn(acc_lo.x, acc_lo.y))), 0.0f};
         }
-        if (lane == 0) red_ss[warp] = make_float2(ss.hi, ss.lo);
-        if (__syncthreads_or(timed_out)) {
-            if constexpr (SCHED == SCHED_PIPE) {
-                if (tid == 0) {
+        if (!WARP_ROWS && lane == 0) red_ss[warp] = make_float2(ss.hi, ss.lo);
+        bool stop;
+        if constexpr (WARP_ROWS) stop = __any_sync(0xFFFFFFFFu, timed_out);
+        else stop = __syncthreads_or(timed_out);
+        if (stop) {
+            if constexpr (RING) {
+                if (issuer) {
                     atomicOr(p.err, ERRF_WAIT_TIMEOUT);
                     // let the copies already issued for later rows land (bounded) before exit
                     int js = stage;
                     uint32_t jp = parity;
                     for (int j = 1; j < S; ++j) {
-                        const long long jrow = row + static_cast<long long>(j) * gridDim.x;
+                        const long long jrow = row + static_cast<long long>(j) * rstep;
                         if (jrow >= p.rows) break;
                         if (++js == S) {
                             js = 0;
@@ -856,11 +880,12 @@ rmsq_row_kernel(const Params p)
             }
             return;
         }
-        if constexpr (SCHED == SCHED_PIPE && !SMEM_S) {
+        if constexpr (RING && !SMEM_S) {
             // Every thread has read this slot (s is held in registers): refill it now with the
             // row S iterations ahead.
-            const long long nrow = row + static_cast<long long>(S) * gridDim.x;
-            if (tid == 0 && nrow < p.rows) {
+            if constexpr (WARP_ROWS) __syncwarp();
+            const long long nrow = row + static_cast<long long>(S) * rstep;
+            if (issuer && nrow < p.rows) {
                 fence_proxy_async_smem();
                 const uint32_t bar = smem_u32(&bars[stage]);
                 mbar_arrive_expect_tx(bar, stage_bytes);
@@ -870,7 +895,13 @@ rmsq_row_kernel(const Params p)
             }
         }
         float rstd;
-        {
+        if constexpr (WARP_ROWS) {
+            // the warp's shuffles left the row's sum (and ONE_BAR's row max) in every lane
+            if constexpr (EXACT)
+                rstd = h_pow2 ? rstd_from_sum_pow2(ss, inv_h, p.eps) : rstd_from_sum(ss, Hf, p.eps);
+            else
+                rstd = __frsqrt_rn(__fadd_rn(__fmul_rn(ss.hi, inv_h), p.eps));
+        } else {
             const float2 part = lane < nwarps ? red_ss[lane] : make_float2(0.0f, 0.0f);
             if constexpr (EXACT) {
                 FF t{part.x, part.y};
@@ -900,7 +931,7 @@ rmsq_row_kernel(const Params p)
         // the residual sum s of vector k (zero past the row end)
         auto get_s = [&](int k) -> uint4 {
             if constexpr (SMEM_S) {
-                const int v = tid + k * T;
+                const int v = rt + k * RT;
                 return v < nv ? ld_shared_v4(stage_addr + v * 16u) : make_uint4(0, 0, 0, 0);
             } else {
                 return s[k];
@@ -963,27 +994,29 @@ rmsq_row_kernel(const Params p)
                     amax = fmaxf(amax, absmax_pairs(yy));
                 }
                 amax = warp_max(amax);
-                if (lane == 0) red_max[warp] = amax;
-                __syncthreads();
-                amax = lane < nwarps ? red_max[lane] : 0.0f;
+                if constexpr (!WARP_ROWS) {
+                    if (lane == 0) red_max[warp] = amax;
+                    __syncthreads();
+                    amax = lane < nwarps ? red_max[lane] : 0.0f;
 #pragma unroll
-                for (int o = 8; o > 0; o >>= 1)
-                    if (o < red_lanes) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
-                amax = __shfl_sync(0xFFFFFFFFu, amax, 0);
+                    for (int o = 8; o > 0; o >>= 1)
+                        if (o < red_lanes) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
+                    amax = __shfl_sync(0xFFFFFFFFu, amax, 0);
+                }
             }
             float scale = __fdiv_rn(fminf(amax, p.scale_ub), 448.0f);
             if (p.scale_dtype == DT_BF16) {
                 uint16_t h;
                 asm("cvt.rn.bf16.f32 %0, %1;" : "=h"(h) : "f"(scale));
                 scale = __uint_as_float(static_cast<uint32_t>(h) << 16);
-                if (tid == 0) static_cast<uint16_t*>(p.scale_out)[row] = h;
+                if (rt == 0) static_cast<uint16_t*>(p.scale_out)[row] = h;
             } else if (p.scale_dtype == DT_FP16) {
                 uint16_t h;
                 asm("cvt.rn.f16.f32 %0, %1;" : "=h"(h) : "f"(scale));
                 asm("cvt.f32.f16 %0, %1;" : "=f"(scale) : "h"(h));
-                if (tid == 0) static_cast<uint16_t*>(p.scale_out)[row] = h;
+                if (rt == 0) static_cast<uint16_t*>(p.scale_out)[row] = h;
             } else {
-                if (tid == 0) static_cast<float*>(p.scale_out)[row] = scale;
+                if (rt == 0) static_cast<float*>(p.scale_out)[row] = scale;
             }
             const bool zero_row = !(scale > 0.0f);
             const float2 inv2 = splat(zero_row ? 0.0f : __frcp_rn(scale));
@@ -991,7 +1024,7 @@ rmsq_row_kernel(const Params p)
             unsigned char* outp = static_cast<unsigned char*>(p.out) + row * p.hidden;
 #pragma unroll
             for (int k = 0; k < VPT; ++k) {
-                const int v = tid + k * T;
+                const int v = rt + k * RT;
                 if (v >= nv) continue;
                 float2 yk[NP];
                 if constexpr (KEEP_Y) {
@@ -1032,7 +1065,7 @@ rmsq_row_kernel(const Params p)
                 }
             }
         } else if constexpr (NV_BLOCKED) {
-            // ---- NVFP4, blocked: thread owns blocks b = tid + kb * T (GROUP vectors each) ---------
+            // ---- NVFP4, blocked: thread owns blocks b = rt + kb * RT (GROUP vectors each) -------
             unsigned char* outp = static_cast<unsigned char*>(p.out) + row * (p.hidden / 2);
             unsigned char* sp_row = static_cast<unsigned char*>(p.scale_out) +
                 (p.swizzled ? (row >> 7) * (static_cast<long long>(p.k_tiles) * 512) +
@@ -1041,7 +1074,7 @@ rmsq_row_kernel(const Params p)
             const int nb = nv / GROUP;
 #pragma unroll
             for (int kb = 0; kb < VPT / GROUP; ++kb) {
-                const int b = tid + kb * T;
+                const int b = rt + kb * RT;
                 if (b >= nb) continue;
                 float2 sw[GROUP][NP];
                 float m = 0.0f;
@@ -1113,7 +1146,7 @@ rmsq_row_kernel(const Params p)
                             : row * p.nsf);
 #pragma unroll
             for (int k = 0; k < VPT; ++k) {
-                const int v = tid + k * T;
+                const int v = rt + k * RT;
                 float2 sw[NP];
                 float m = 0.0f;
                 sw_pairs(k, sw);
@@ -1162,9 +1195,16 @@ rmsq_row_kernel(const Params p)
         }
         if constexpr (SMEM_S) {
             // Every thread is done with this slot: refill it with the row S iterations ahead.
-            __syncthreads();
-            const long long nrow = row + static_cast<long long>(S) * gridDim.x;
-            if (tid == 0 && nrow < p.rows) {
+            // (Each lane wrote s into the slot; in the row-per-warp schedule every lane orders
+            // its writes before the refill's async-proxy writes.)
+            if constexpr (WARP_ROWS) {
+                fence_proxy_async_smem();
+                __syncwarp();
+            } else {
+                __syncthreads();
+            }
+            const long long nrow = row + static_cast<long long>(S) * rstep;
+            if (issuer && nrow < p.rows) {
                 fence_proxy_async_smem();
                 const uint32_t bar = smem_u32(&bars[stage]);
                 mbar_arrive_expect_tx(bar, stage_bytes);
@@ -1173,7 +1213,7 @@ rmsq_row_kernel(const Params p)
                     bulk_load(stage_addr + row_bytes, rg + nrow * nv, row_bytes, bar, policy);
             }
         }
-        if constexpr (SCHED == SCHED_PIPE) {
+        if constexpr (RING) {
             if (++stage == S) {
                 stage = 0;
                 parity ^= 1u;

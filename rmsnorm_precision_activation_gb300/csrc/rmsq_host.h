@@ -14,16 +14,17 @@ struct Plan {
     int dt;            // DT_*
     bool res;          // residual present
     int vpt;           // 16-byte vectors per thread per row: 1, 2, 4 or 8
-    int sched;         // SCHED_PIPE or SCHED_REG
-    int threads;       // CTA size (multiple of 32)
-    int stages;        // SCHED_PIPE ring depth
+    int sched;         // SCHED_PIPE, SCHED_REG or SCHED_WARP
+    int threads;       // CTA size (multiple of 32); SCHED_WARP: 32 x rows in flight per CTA
+    int stages;        // ring depth (SCHED_PIPE: per CTA, SCHED_WARP: per warp)
     int smem;          // dynamic shared memory bytes
     int ctas_per_sm;   // cap on resident CTAs per SM (0: occupancy limit)
     bool w16;          // 16-bit input and weight_offset 0: products from packed halves
 };
 
 // Launch `fn` (a rmsq_row_kernel instantiation) with the plan: sets the dynamic shared memory
-// limit once per function and device, sizes a persistent grid of min(rows, CTAs per SM x SMs).
+// limit once per function and device, sizes a persistent grid of CTAs per SM x SMs (no more CTAs
+// than it takes to give each one a row; a row-per-warp CTA takes one row per warp).
 cudaError_t run_kernel(const void* fn, const Plan& plan, const Params& p, cudaStream_t stream);
 
 // Per-mode dispatch on (dtype, residual, vpt, schedule); defined in rmsq_<mode>.cu.
@@ -52,8 +53,11 @@ cudaError_t dispatch_amax(const Plan& plan, const Params& p, cudaStream_t stream
     template <int DT, bool RES, int VPT>                                                          \
     static cudaError_t NAME##_sched(const Plan& pl, const Params& p, cudaStream_t st)             \
     {                                                                                             \
-        return pl.sched == SCHED_PIPE ? NAME##_w16<DT, RES, VPT, SCHED_PIPE>(pl, p, st)           \
-                                      : NAME##_w16<DT, RES, VPT, SCHED_REG>(pl, p, st);           \
+        switch (pl.sched) {                                                                       \
+        case SCHED_PIPE: return NAME##_w16<DT, RES, VPT, SCHED_PIPE>(pl, p, st);                  \
+        case SCHED_WARP: return NAME##_w16<DT, RES, VPT, SCHED_WARP>(pl, p, st);                  \
+        default: return NAME##_w16<DT, RES, VPT, SCHED_REG>(pl, p, st);                           \
+        }                                                                                         \
     }                                                                                             \
     template <int DT, bool RES>                                                                   \
     static cudaError_t NAME##_vpt(const Plan& pl, const Params& p, cudaStream_t st)               \
