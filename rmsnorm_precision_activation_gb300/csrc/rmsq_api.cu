@@ -136,11 +136,18 @@ cudaError_t run_kernel(const void* fn, const Plan& pl, const Params& p, cudaStre
 static int elems_per_vec(int dt) { return dt == DT_F32 ? 4 : 8; }
 
 // Pick vectors per thread, CTA size, schedule, ring depth and residency for one call.
-// From on-GPU sweeps (GB300): each thread takes the power of two nearest nv / 128 vectors of 16
-// bytes per row (FP8 without W16 at most 4, so y stays in registers), except FP4 with a residual:
-// 2 vectors per thread up to hidden 4096 (bf16) and 8 above; a two-row ring per CTA (three for
-// short FP4 rows); few CTAs per SM for FP4 with a residual (4 / 3 / 2 as rows grow) and the W16
-// FP8 kernel (4), more for FP4 without one (8) and the other FP8 kernels (6).
+// From on-GPU sweeps (GB300), with nv = 16-byte vectors per row:
+//  - Short rows (nv <= 256 without a residual, nv <= 64 with one) take the row-per-warp
+//    schedule: 8 warps per CTA, a two-row ring per warp, as many CTAs as fit.
+//  - Otherwise a CTA per row. Each thread takes the power of two nearest nv / 128 vectors
+//    (FP8 without W16 at most 4, so y stays in registers), with two exceptions:
+//    - FP4 with a residual: 2 vectors per thread up to hidden 4096 (bf16), 8 above;
+//    - FP8 rows of up to 256 vectors: 4 vectors per thread and about 12 warps per SM.
+//  - A two-row ring per CTA, three for FP4 rows of 256-511 vectors with a residual.
+//  - CTAs per SM:
+//    - FP4 with a residual: 8 / 4 / 3 / 2 as rows grow;
+//    - the W16 FP8 kernel: 4; the other FP8 kernels: 6;
+//    - FP4 without a residual: 8.
 static bool make_plan(int mode, int dt, bool res, bool w16, int hidden, const DeviceInfo& di,
                       Plan& pl)
 {
@@ -156,14 +163,15 @@ static bool make_plan(int mode, int dt, bool res, bool w16, int hidden, const De
     // 16-bit input) and each warp keeps its own two-row ring.
     const int warp_red = kRedFloatsWarp * 4;
     const bool warp_fits = nv <= 256 && 2 * stage + warp_red + 16 <= di.smem_optin;
-    if (warp_fits && forced == SCHED_WARP) {
+    const bool warp_auto = res ? nv <= 64 : nv <= 256;
+    if (warp_fits && (forced == SCHED_WARP || (forced == 0 && warp_auto))) {
         int vpt = 1;
         while (32 * vpt < nv) vpt *= 2;
         if (mode == MODE_NVFP4 && vpt < group) vpt = group;
         const int tv = g_tune_vpt.load();
         if (tv > vpt) vpt = tv;
         int warps = g_tune_warps.load();
-        if (warps == 0) warps = stage <= 2048 ? 4 : (stage <= 4096 ? 2 : 1);
+        if (warps == 0) warps = 8;
         int stages = g_tune_stages.load();
         if (stages == 0) stages = 2;
         auto bytes = [&](int w, int st) { return w * st * stage + warp_red + w * st * 8; };
@@ -183,12 +191,13 @@ static bool make_plan(int mode, int dt, bool res, bool w16, int hidden, const De
         if (mode != MODE_FP8 && mode != MODE_AMAX && res) {
             // FP4 with a residual (bandwidth-bound): ~128 threads for short rows, 256 at 4096,
             // 8 vectors per thread from 5120 on
-            vpt = nv >= 640 ? 8 : (nv >= 512 ? 2 : (nv >= 256 ? 2 : 1));
+            vpt = nv >= 640 ? 8 : 2;
         } else {
             // the power of two nearest nv / 128 vectors per thread
             vpt = 1;
             while (vpt < 8 && 2 * nv > 3 * 128 * vpt) vpt *= 2;
             if (mode == MODE_FP8 && !w16 && vpt > 4) vpt = 4;
+            if (mode == MODE_FP8 && nv <= 256) vpt = 4;
         }
         while (vpt < 8 && (nv + vpt - 1) / vpt > 512) vpt *= 2;
         // NVFP4 threads own whole 16-element scale blocks (2 vectors, 4 for fp32 input)
@@ -204,13 +213,13 @@ static bool make_plan(int mode, int dt, bool res, bool w16, int hidden, const De
     pl.sched = (forced == SCHED_REG || !pipe_fits) ? SCHED_REG : SCHED_PIPE;
     pl.ctas_per_sm = g_tune_ctas.load();
     if (pl.ctas_per_sm == 0) {
-        if (mode == MODE_FP8) pl.ctas_per_sm = w16 ? 4 : 6;
+        if (mode == MODE_FP8) pl.ctas_per_sm = nv <= 256 ? 384 / threads : (w16 ? 4 : 6);
         else if (!res) pl.ctas_per_sm = 8;
-        else pl.ctas_per_sm = nv < 512 ? 4 : (nv < 1024 ? 3 : 2);
+        else pl.ctas_per_sm = nv < 256 ? 8 : (nv < 512 ? 4 : (nv < 1024 ? 3 : 2));
     }
     if (pl.sched == SCHED_PIPE) {
         int stages = g_tune_stages.load();
-        if (stages == 0) stages = (mode != MODE_FP8 && res && nv < 512) ? 3 : 2;
+        if (stages == 0) stages = (mode != MODE_FP8 && res && nv >= 256 && nv < 512) ? 3 : 2;
         while (stages > 2 && stages * stage + red_bytes + stages * 8 > di.smem_optin) --stages;
         pl.stages = stages;
         pl.smem = static_cast<int>(stages * stage) + red_bytes + stages * 8;

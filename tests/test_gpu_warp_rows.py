@@ -9,7 +9,8 @@ import pytest
 import torch
 
 import workloads as W
-from gpu_common import check_fp8, check_mxfp4, check_nvfp4, inputs, rq, sample_rows, schedule
+from gpu_common import (check_fp8, check_mxfp4, check_nvfp4, inputs, oracle_global_scale, rq,
+                        sample_rows, schedule)
 
 pytestmark = pytest.mark.gpu
 
@@ -95,6 +96,37 @@ def test_warp_rows_cta_sizes(warps):
             check_mxfp4(wm, dm)
     finally:
         rq().rmsq_set_row_warps(0)
+
+
+@pytest.mark.parametrize("sched", [0, WARP])
+@pytest.mark.parametrize("residual", [False, True])
+def test_warp_rows_global_scale_prepass(sched, residual):
+    # the NVFP4 global-amax pre-pass (one atomic max per warp) on short rows
+    w = W.Workload("custom", "nvfp4", 3001, 1024, "bf16", residual)
+    d = inputs(w, seed=31 + residual)
+    gs = float(oracle_global_scale(w, d))
+    with schedule(sched):
+        dev = rq().rmsnorm_nvfp4_global_scale(d["input"], d["gamma"], residual=d["residual"],
+                                              epsilon=w.eps)
+    torch.cuda.synchronize()
+    got = float(dev.cpu()[0])
+    assert abs(got - gs) <= 2e-6 * gs, (got, gs)
+
+
+@pytest.mark.parametrize("mode", ["fp8", "nvfp4", "mxfp4"])
+@pytest.mark.parametrize("rows,hidden,residual", [(5000, 256, True), (4000, 512, True),
+                                                   (3000, 1024, True), (3000, 2048, False),
+                                                   (2000, 2048, True)])
+def test_short_rows_automatic_plan(mode, rows, hidden, residual):
+    # whatever schedule the planner picks for short rows
+    w = W.Workload("custom", mode, rows, hidden, "bf16", residual, scale_ub=1200.0)
+    d = inputs(w, seed=rows + hidden)
+    if mode == "fp8":
+        check_fp8(w, d)
+    elif mode == "nvfp4":
+        check_nvfp4(w, d, 1.5)
+    else:
+        check_mxfp4(w, d)
 
 
 def test_warp_rows_fall_back_for_wide_rows():
