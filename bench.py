@@ -202,12 +202,21 @@ class Step:
 
 
 def barrier_max(value, world):
+    """The maximum of `value` over all ranks (NCCL on the GPUs, or gloo on the CPU)."""
     if world == 1:
         return value
     import torch.distributed as dist
-    t = torch.tensor([value], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def replica_throughput(step_bytes, steps, world, local_ms):
+    """Whole-job GB/s of `world` independent replicas, each moving step_bytes per step: all
+    ranks' bytes over the slowest rank's time. Returns (GB/s, slowest rank's ms)."""
+    ms = barrier_max(local_ms, world)
+    return step_bytes * steps * world / (ms * 1e-3) / 1e9, ms
 
 
 def barrier(world):
@@ -256,15 +265,13 @@ def run_ours(args):
         torch.cuda.synchronize()
     barrier(world)
     launches = rq.rmsq_launch_count() - launches0
-    total_ms = barrier_max(t0.elapsed_time(t1), world)
+    value, total_ms = replica_throughput(step.step_bytes, K, world, t0.elapsed_time(t1))
     per_mode_ms = {m: statistics.mean(a.elapsed_time(b) for a, b in ev[m]) for m in MODES}
     assert rq.rmsq_device_status() == 0
 
     # ---- end to end through the public API with host buffers -------------------------------
     e2e = run_e2e(rq, step, device, max(3, min(K, 10)), world)
 
-    bytes_all = step.step_bytes * K * world
-    value = bytes_all / (total_ms * 1e-3) / 1e9
     rows_per_s = 3 * rows * K * world / (total_ms * 1e-3)
     dom = max(per_mode_ms, key=per_mode_ms.get)
     dom_gbs = step.bytes[dom] / (per_mode_ms[dom] * 1e-3) / 1e9
@@ -344,8 +351,8 @@ def run_e2e(rq, step, device, K, world):
         one()
     b.record(stream)
     torch.cuda.synchronize()
-    ms = barrier_max(a.elapsed_time(b), world)
-    return {"value": round(step.step_bytes * K * world / (ms * 1e-3) / 1e9, 1), "unit": "GB/s",
+    value, ms = replica_throughput(step.step_bytes, K, world, a.elapsed_time(b))
+    return {"value": round(value, 1), "unit": "GB/s",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "ms_per_step": round(ms / K, 4), "steps": K}
 
@@ -446,6 +453,64 @@ def run_reference(args):
 # per-workload report
 # ------------------------------------------------------------------------------------------
 
+def oracle_rate(w, seconds, threads=None):
+    """The oracle, as it stands, on a bounded row sample of workload w: GB/s of the sample's
+    algorithmic bytes and rows/s, on all host cores unless `threads` is given. The sample is
+    grown until it runs for about `seconds`; it is timed best of 3 when it moves under 1 GB, once
+    otherwise."""
+    import dataclasses
+    import numpy as np
+    import oracle
+    oracle.build()
+    odt = {"bf16": oracle.BF16, "fp16": oracle.FP16}[w.dtype]
+    kw = dict(dtype=odt, eps=w.eps, weight_offset=w.weight_offset, threads=threads)
+
+    def sample(n):
+        ws = dataclasses.replace(w, rows=n)
+        d = W.generate(ws, seed=0)
+        x, g = W.bits(d["input"]), W.bits(d["gamma"])
+        r = None if d["residual"] is None else W.bits(d["residual"])
+        if w.mode == "fp8":
+            return ws, lambda: oracle.quant_fp8(x, r, g, scale_ub=w.scale_ub, **kw)
+        if w.mode == "nvfp4":
+            y = oracle.rmsnorm(x, r, g, dtype=odt, eps=w.eps, weight_offset=w.weight_offset)["y"]
+            gs = float(oracle.nvfp4_global_scale(np.abs(y).max()))
+            return ws, lambda: oracle.quant_nvfp4(x, r, g, gs, **kw)
+        return ws, lambda: oracle.quant_mxfp4(x, r, g, **kw)
+
+    def timed(fn):
+        t = time.perf_counter()
+        fn()
+        return time.perf_counter() - t
+
+    n = min(w.rows, 16)
+    while True:                      # grow the sample until it runs for about `seconds`
+        ws, fn = sample(n)
+        dt = timed(fn)
+        if dt >= seconds / 2 or n >= w.rows:
+            break
+        n = int(min(w.rows, max(2 * n, n * seconds / max(dt, 1e-4))))
+    nbytes = ws.algorithmic_bytes()
+    if nbytes < 1e9:
+        dt = min([dt] + [timed(fn) for _ in range(2)])
+    return {"gbs": round(nbytes / dt / 1e9, 4), "rows_per_s": round(n / dt, 1),
+            "threads": threads or oracle.cores(), "sample_rows": n, "seconds": round(dt, 3)}
+
+
+def host_cpu():
+    """CPU model name and usable cores of this host, for the oracle columns."""
+    model = ""
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith(("model name", "cpu model")):
+                    model = line.split(":", 1)[1].strip()
+                    break
+    except OSError:
+        pass
+    return {"model": model or os.uname().machine, "cores": len(os.sched_getaffinity(0))}
+
+
 def report_workloads():
     names = [("fp8_small", None, None), ("fp8_residual", None, None), ("fp8_gemma", None, None),
              ("nvfp4", None, None)]
@@ -459,6 +524,7 @@ def run_report(args):
     import rmsnorm_precision_activation_gb300 as rq
     torch.cuda.set_device(0)
     peak, _ = measured_peak()
+    cpu = host_cpu()
     flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
     only = set(args.only.split(",")) if args.only else None
     for name, rows, hidden in report_workloads():
@@ -489,13 +555,19 @@ def run_report(args):
             times.append(a.elapsed_time(b))
         us = statistics.median(times) * 1e3
         gbs = w.algorithmic_bytes() / (us * 1e-6) / 1e9
-        print(json.dumps({"workload": name, "shape": [w.rows, w.hidden], "io_dtype": w.dtype,
-                          "mode": w.mode, "residual": w.residual, "us": round(us, 2),
-                          "algorithmic_bytes": w.algorithmic_bytes(), "gbs": round(gbs, 1),
-                          "rows_per_s": round(w.rows / (us * 1e-6)),
-                          "frac_of_measured": round(gbs / peak, 4),
-                          "pct_of_8tbs": round(100 * gbs / NOMINAL_HBM_GBS, 2)}), flush=True)
+        line = {"workload": name, "shape": [w.rows, w.hidden], "io_dtype": w.dtype,
+                "mode": w.mode, "residual": w.residual, "us": round(us, 2),
+                "algorithmic_bytes": w.algorithmic_bytes(), "gbs": round(gbs, 1),
+                "rows_per_s": round(w.rows / (us * 1e-6)),
+                "frac_of_measured": round(gbs / peak, 4),
+                "pct_of_8tbs": round(100 * gbs / NOMINAL_HBM_GBS, 2)}
         del outs, d
+        if args.oracle_seconds > 0:
+            # the oracle beside the GPU figure: a reported baseline, not the target
+            line["oracle"] = {"all_cores": oracle_rate(w, args.oracle_seconds), "cpu": cpu}
+            if name in ("fp8_small", "fp8_residual"):
+                line["oracle"]["one_thread"] = oracle_rate(w, args.oracle_seconds, threads=1)
+        print(json.dumps(line), flush=True)
 
 
 # ------------------------------------------------------------------------------------------
@@ -570,6 +642,9 @@ def main():
     ap.add_argument("--no-pdl", action="store_true",
                     help="launch without programmatic dependent launch (for comparison)")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--oracle-seconds", type=float, default=0.3,
+                    help="--report: time the oracle on a row sample of each workload for about "
+                         "this long (0: skip)")
     ap.add_argument("--ncu-table", default="", metavar="CSV",
                     help="print the per-workload DRAM table from the ncu CSV of a --report run "
                          "(same --only / --report-reps); needs no GPU")
