@@ -125,10 +125,14 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
     }
 }
 
-__device__ __forceinline__ uint64_t l2_evict_first_policy()
+// L2 priority of the row loads. Normal priority (rather than evict-first) lets the kernel's own
+// dirty output lines leave L2 while it runs instead of piling up until it ends: measured on
+// GB300, the ncu DRAM throughput of the NVFP4 / MXFP4 launches rises by 3-4 points and the long
+// MXFP4 launches get 3 % shorter.
+__device__ __forceinline__ uint64_t l2_evict_normal_policy()
 {
     uint64_t pol;
-    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(pol));
     return pol;
 }
 
@@ -708,9 +712,9 @@ rmsq_row_kernel(const Params p)
 
     uint64_t policy = 0;
     if constexpr (RING) {
-        policy = l2_evict_first_policy();
-        if (tid == 0) {
-            for (int s = 0; s < S * nrings; ++s) mbar_init(smem_u32(&bars_all[s]), 1);
+        policy = l2_evict_normal_policy();
+        if (issuer) {
+            for (int s = 0; s < S; ++s) mbar_init(smem_u32(&bars[s]), 1);
             fence_mbar_init();
         }
     }
@@ -719,19 +723,8 @@ rmsq_row_kernel(const Params p)
     // visible, then let the next one start its own prologue while this grid runs.
     asm volatile("griddepcontrol.wait;" ::: "memory");
     asm volatile("griddepcontrol.launch_dependents;");
-
-    float gs = 1.0f, gs_over_6 = 0.0f;
-    if constexpr (MODE == MODE_NVFP4) {
-        gs = __ldg(p.gs);
-        gs_over_6 = __fdiv_rn(gs, 6.0f);
-        // factor[c] = gs / dec(c) for every positive E4M3 code (0 for code 0 and for NaN)
-        for (int c = tid; c < 128; c += T) {
-            const float ds = e4m3_value(static_cast<uint32_t>(c));
-            nv_factor[c] = (c == 0 || c == 0x7F) ? 0.0f : __fdiv_rn(gs, ds);
-        }
-    }
-    if constexpr (RING || MODE == MODE_NVFP4) __syncthreads();
     if constexpr (RING) {
+        // the ring's first rows, issued by the thread that initialised its barriers
         if (issuer) {
             for (int s = 0; s < S; ++s) {
                 const long long row = row0 + static_cast<long long>(s) * rstep;
@@ -744,6 +737,19 @@ rmsq_row_kernel(const Params p)
             }
         }
     }
+
+    float gs = 1.0f, gs_over_6 = 0.0f;
+    if constexpr (MODE == MODE_NVFP4) {
+        gs = __ldg(p.gs);
+        gs_over_6 = __fdiv_rn(gs, 6.0f);
+        // factor[c] = gs / dec(c) for every positive E4M3 code (0 for code 0 and for NaN)
+        for (int c = tid; c < 128; c += T) {
+            const float ds = e4m3_value(static_cast<uint32_t>(c));
+            nv_factor[c] = (c == 0 || c == 0x7F) ? 0.0f : __fdiv_rn(gs, ds);
+        }
+    }
+    // the barrier initialisations and the factor table are visible to every thread after this
+    if constexpr (RING || MODE == MODE_NVFP4) __syncthreads();
 
     const float2 offset2 = splat(p.offset);
     GammaRegs<E, VPT, !W16 && VPT <= 4> G;
