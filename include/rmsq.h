@@ -158,7 +158,8 @@ const char* rmsq_status_string(rmsq_status status);
  * rmsq_device_status -- errors raised on the device since the last call, for the current device.
  * Every wait inside a kernel (on a bulk-copy barrier) is bounded in time; a wait that runs out
  * sets a flag, the kernel stops cleanly and its outputs are incomplete. This call synchronises
- * the device, returns RMSQ_ERR_TIMEOUT if a flag was set (RMSQ_OK otherwise) and clears it.
+ * the device, returns RMSQ_ERR_TIMEOUT if a flag was set (RMSQ_OK otherwise) and clears it,
+ * together with the row counters a stopped launch may have left behind.
  * ------------------------------------------------------------------------------------------- */
 rmsq_status rmsq_device_status(void);
 
@@ -178,6 +179,10 @@ rmsq_status rmsq_device_status(void);
  *                    RMSQ_ERR_SHAPE.
  * rmsq_set_row_warps  warps per CTA of the row-per-warp schedule (0 = automatic, at most 16).
  *                    Returns RMSQ_ERR_VALUE out of range.
+ * rmsq_set_dynamic_rows  the CTA-per-row schedule hands the last quarter of its rows out one at a
+ *                    time from a per-launch counter in the library's device memory, so CTAs on
+ *                    SMs that get more HBM bandwidth take more rows (default). 0 deals every row
+ *                    out round-robin. Returns the previous setting.
  * rmsq_set_pdl      kernels are launched with programmatic dependent launch by default (a
  *                    launch may be scheduled while the previous kernel on the stream finishes; it
  *                    waits for that kernel before touching global memory). 0 turns this off for
@@ -193,6 +198,7 @@ rmsq_status rmsq_device_status(void);
 int rmsq_set_schedule(int schedule);
 rmsq_status rmsq_set_tuning(int stages, int ctas_per_sm, int vectors_per_thread);
 rmsq_status rmsq_set_row_warps(int warps_per_cta);
+int rmsq_set_dynamic_rows(int enable);
 int rmsq_set_pdl(int enable);
 void rmsq_set_wait_timeout_ns(uint64_t timeout_ns);
 rmsq_status rmsq_selftest_wait_timeout(uint64_t timeout_ns, void* stream);

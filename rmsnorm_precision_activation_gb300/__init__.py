@@ -43,6 +43,7 @@ SIGNATURES = {
     "rmsq_set_schedule": ([_I], _I),
     "rmsq_set_tuning": ([_I, _I, _I], _I),
     "rmsq_set_row_warps": ([_I], _I),
+    "rmsq_set_dynamic_rows": ([_I], _I),
     "rmsq_set_pdl": ([_I], _I),
     "rmsq_set_wait_timeout_ns": ([_U64], None),
     "rmsq_selftest_wait_timeout": ([_U64, _P], _I),
@@ -234,6 +235,10 @@ def rmsq_set_tuning(stages: int = 0, ctas_per_sm: int = 0, vectors_per_thread: i
 
 def rmsq_set_row_warps(warps_per_cta: int = 0):
     _check(lib().rmsq_set_row_warps(int(warps_per_cta)), "rmsq_set_row_warps")
+
+
+def rmsq_set_dynamic_rows(enable: bool) -> bool:
+    return bool(lib().rmsq_set_dynamic_rows(int(bool(enable))))
 
 
 def rmsq_set_pdl(enable: bool) -> bool:

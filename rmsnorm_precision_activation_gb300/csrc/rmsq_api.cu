@@ -14,6 +14,17 @@ namespace rmsq {
 // Device-side error word (bit ERRF_WAIT_TIMEOUT: a bounded wait ran out). One per device.
 static __device__ unsigned int g_err_word;
 
+// Row counters of the dynamic row tail, one per launch, taken in turn from a pool of
+// kCounterSlots slots (32 bytes apart) that lives as long as the library. The thread holding a
+// launch's last ticket sets its counter back to 0, so a slot is clean when its turn comes again:
+// launches in one stream run in order, and launches on other streams would have to be more than
+// kCounterSlots launches apart in issue order and still running together to meet on a slot. A
+// launch stopped by a timed-out wait can leave its counter behind; rmsq_device_status clears the
+// pool when it reports that.
+constexpr int kCounterSlots = 4096;
+static __device__ __align__(256) unsigned int g_row_counters[kCounterSlots * 8];
+static std::atomic<unsigned long long> g_counter_seq{0};
+
 static std::atomic<int> g_schedule{0};
 static std::atomic<int> g_tune_stages{0};
 static std::atomic<int> g_tune_ctas{0};
@@ -22,6 +33,7 @@ static std::atomic<int> g_tune_warps{0};
 static std::atomic<unsigned long long> g_timeout_ns{2000000000ull};
 static std::atomic<unsigned long long> g_launches{0};
 static std::atomic<bool> g_pdl{true};
+static std::atomic<bool> g_dynamic_rows{true};
 
 constexpr int kMaxDevices = 64;
 
@@ -31,6 +43,7 @@ struct DeviceInfo {
     int sms = 0;
     int smem_optin = 0;
     unsigned int* err = nullptr;
+    unsigned int* counters = nullptr;
 };
 
 static std::mutex g_mu;
@@ -55,9 +68,12 @@ static const DeviceInfo* device_info()
                   cudaDeviceGetAttribute(&d.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) ==
                       cudaSuccess;
         void* addr = nullptr;
+        void* ctr = nullptr;
         ok = ok && major == 10 && minor == 3 &&
-             cudaGetSymbolAddress(&addr, g_err_word) == cudaSuccess;
+             cudaGetSymbolAddress(&addr, g_err_word) == cudaSuccess &&
+             cudaGetSymbolAddress(&ctr, g_row_counters) == cudaSuccess;
         d.err = static_cast<unsigned int*>(addr);
+        d.counters = static_cast<unsigned int*>(ctr);
         d.usable = ok;
         d.ready = true;
         if (!ok) cudaGetLastError();
@@ -111,7 +127,22 @@ cudaError_t run_kernel(const void* fn, const Plan& pl, const Params& p, cudaStre
     const long long rows_per_cta = pl.sched == SCHED_WARP ? pl.threads / 32 : 1;
     if (grid > (p.rows + rows_per_cta - 1) / rows_per_cta)
         grid = (p.rows + rows_per_cta - 1) / rows_per_cta;
-    void* args[] = {const_cast<Params*>(&p)};
+    // Dynamic row tail (CTA-per-row ring schedule): SMs do not get equal shares of HBM
+    // bandwidth, so with rows dealt out round-robin the slowest SM sets the end of the launch
+    // (measured on GB300: the last CTA ended 11-17 us after the median one on 130-170 us
+    // launches). Each CTA takes its first 3/4 of an equal share round-robin and the rest one
+    // row at a time from the launch's counter.
+    Params q = p;
+    const long long procs = grid * rows_per_cta;
+    q.rowctr = nullptr;
+    q.rows_static = p.rows;
+    if (g_dynamic_rows.load() && pl.sched == SCHED_PIPE && di.counters != nullptr && p.rows >= 2 * procs &&
+        p.rows < (1LL << 31)) {
+        const unsigned long long slot = g_counter_seq.fetch_add(1) % kCounterSlots;
+        q.rowctr = di.counters + slot * 8;
+        q.rows_static = p.rows / procs * 3 / 4 * procs;
+    }
+    void* args[] = {&q};
     // Programmatic dependent launch: the kernel may be scheduled while the previous kernel on the
     // stream finishes; it waits (griddepcontrol.wait) before touching global memory.
     cudaLaunchConfig_t cfg = {};
@@ -141,11 +172,13 @@ static int elems_per_vec(int dt) { return dt == DT_F32 ? 4 : 8; }
 //    schedule: 8 warps per CTA, a two-row ring per warp, as many CTAs as fit.
 //  - Otherwise a CTA per row. Each thread takes the power of two nearest nv / 128 vectors
 //    (FP8 without W16 at most 4, so y stays in registers), with two exceptions:
-//    - FP4 with a residual: 2 vectors per thread up to hidden 4096 (bf16), 8 above;
+//    - FP4 with a residual: 2 vectors per thread up to 1024 vectors per row, then as many as
+//      make 512 threads (NVFP4 rows of up to 512 vectors: 4);
 //    - FP8 rows of up to 256 vectors: 4 vectors per thread and about 12 warps per SM.
-//  - A two-row ring per CTA, three for FP4 rows of 256-511 vectors with a residual.
-//  - CTAs per SM:
-//    - FP4 with a residual: 8 / 4 / 3 / 2 as rows grow;
+//  - A two-row ring per CTA; three for FP4 rows with a residual of 256-511 vectors, or of
+//    2048 vectors and more (one CTA per SM then).
+//  - CTAs per SM (shared memory permitting):
+//    - FP4 with a residual: 8;
 //    - the W16 FP8 kernel: 4; the other FP8 kernels: 6;
 //    - FP4 without a residual: 8.
 static bool make_plan(int mode, int dt, bool res, bool w16, int hidden, const DeviceInfo& di,
@@ -162,7 +195,7 @@ static bool make_plan(int mode, int dt, bool res, bool w16, int hidden, const De
     // Row per warp: a warp holds the row in at most 8 vectors per lane (hidden <= 2048 for
     // 16-bit input) and each warp keeps its own two-row ring.
     const int warp_red = kRedFloatsWarp * 4;
-    const bool warp_fits = nv <= 256 && 2 * stage + warp_red + 16 <= di.smem_optin;
+    const bool warp_fits = nv <= 256 && 2 * stage + warp_red + 32 <= di.smem_optin;
     const bool warp_auto = res ? nv <= 64 : nv <= 256;
     if (warp_fits && (forced == SCHED_WARP || (forced == 0 && warp_auto))) {
         int vpt = 1;
@@ -174,7 +207,7 @@ static bool make_plan(int mode, int dt, bool res, bool w16, int hidden, const De
         if (warps == 0) warps = 8;
         int stages = g_tune_stages.load();
         if (stages == 0) stages = 2;
-        auto bytes = [&](int w, int st) { return w * st * stage + warp_red + w * st * 8; };
+        auto bytes = [&](int w, int st) { return w * st * stage + warp_red + w * st * 16; };
         while (stages > 2 && bytes(warps, stages) > di.smem_optin) --stages;
         while (warps > 1 && bytes(warps, stages) > di.smem_optin) warps /= 2;
         pl.sched = SCHED_WARP;
@@ -191,7 +224,9 @@ static bool make_plan(int mode, int dt, bool res, bool w16, int hidden, const De
         if (mode != MODE_FP8 && mode != MODE_AMAX && res) {
             // FP4 with a residual (bandwidth-bound): ~128 threads for short rows, 256 at 4096,
             // 8 vectors per thread from 5120 on
-            vpt = nv >= 640 ? 8 : 2;
+            vpt = 2;
+            while (vpt < 8 && nv > 512 * vpt) vpt *= 2;
+            if (mode == MODE_NVFP4 && nv <= 512) vpt = 4;
         } else {
             // the power of two nearest nv / 128 vectors per thread
             vpt = 1;
@@ -209,20 +244,22 @@ static bool make_plan(int mode, int dt, bool res, bool w16, int hidden, const De
     pl.threads = threads;
 
     const int red_bytes = kRedFloats * 4;
-    const bool pipe_fits = 2 * stage + red_bytes + 2 * 8 <= di.smem_optin;
+    const bool pipe_fits = 2 * stage + red_bytes + 2 * 16 <= di.smem_optin;
     pl.sched = (forced == SCHED_REG || !pipe_fits) ? SCHED_REG : SCHED_PIPE;
     pl.ctas_per_sm = g_tune_ctas.load();
     if (pl.ctas_per_sm == 0) {
         if (mode == MODE_FP8) pl.ctas_per_sm = nv <= 256 ? 384 / threads : (w16 ? 4 : 6);
         else if (!res) pl.ctas_per_sm = 8;
-        else pl.ctas_per_sm = nv < 256 ? 8 : (nv < 512 ? 4 : (nv < 1024 ? 3 : 2));
+        else pl.ctas_per_sm = 8;
     }
     if (pl.sched == SCHED_PIPE) {
         int stages = g_tune_stages.load();
-        if (stages == 0) stages = (mode != MODE_FP8 && res && nv >= 256 && nv < 512) ? 3 : 2;
-        while (stages > 2 && stages * stage + red_bytes + stages * 8 > di.smem_optin) --stages;
+        if (stages == 0)
+            stages = (mode != MODE_FP8 && res && ((nv >= 256 && nv < 512) || nv >= 2048)) ? 3 : 2;
+        // ring slots, reduction area, then per slot an mbarrier and the slot's row number
+        while (stages > 2 && stages * stage + red_bytes + stages * 16 > di.smem_optin) --stages;
         pl.stages = stages;
-        pl.smem = static_cast<int>(stages * stage) + red_bytes + stages * 8;
+        pl.smem = static_cast<int>(stages * stage) + red_bytes + stages * 16;
     } else {
         pl.stages = 0;
         pl.smem = red_bytes;
@@ -489,6 +526,7 @@ extern "C" rmsq_status rmsq_device_status(void)
     if (word != 0) {
         const unsigned int zero = 0;
         cudaMemcpyToSymbol(g_err_word, &zero, sizeof zero);
+        cudaMemset(di->counters, 0, sizeof(unsigned int) * kCounterSlots * 8);
         return RMSQ_ERR_TIMEOUT;
     }
     return RMSQ_OK;
@@ -517,6 +555,11 @@ extern "C" rmsq_status rmsq_set_row_warps(int warps_per_cta)
     if (warps_per_cta < 0 || warps_per_cta > 16) return RMSQ_ERR_VALUE;
     g_tune_warps = warps_per_cta;
     return RMSQ_OK;
+}
+
+extern "C" int rmsq_set_dynamic_rows(int enable)
+{
+    return g_dynamic_rows.exchange(enable != 0) ? 1 : 0;
 }
 
 extern "C" int rmsq_set_pdl(int enable)

@@ -57,6 +57,11 @@ struct Params {
     int k_tiles;              // FP4 swizzled: 4-scale tiles per row
     int stages;               // SCHED_PIPE / SCHED_WARP: ring depth (per ring)
     unsigned long long timeout_ns;
+    // Ring schedules: rows below rows_static go round-robin over the row processors (CTAs, or
+    // warps for SCHED_WARP); the rest are handed out one at a time from the counter *rowctr,
+    // which starts at 0 and is left at 0. rowctr may be null, with rows_static = rows.
+    unsigned int* rowctr;
+    long long rows_static;
 };
 
 // ------------------------------------------------------------------------------------------
@@ -83,6 +88,12 @@ __device__ __forceinline__ void fence_mbar_init()
 __device__ __forceinline__ void fence_proxy_async_smem()
 {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// Completes the barrier's phase without a copy (count 1): the slot carries no row.
+__device__ __forceinline__ void mbar_arrive(uint32_t bar)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes)
@@ -634,8 +645,9 @@ struct GammaRegs<E, VPT, false> {
 };
 
 // Shared memory after the stage rings: [2][32] float2 sum-of-squares partials, [2][32] row
-// maxima, [128] NVFP4 element factors gs / dec(s) indexed by the E4M3 block-scale code. The
-// row-per-warp schedule reduces in registers and keeps only the factor table.
+// maxima, [128] NVFP4 element factors gs / dec(s) indexed by the E4M3 block-scale code (the
+// row-per-warp schedule reduces in registers and keeps only the factor table), then per ring
+// [stages] mbarriers and [stages] row numbers of the slots.
 constexpr int kRedFloats = 2 * 32 * 2 + 2 * 32 + 128;
 constexpr int kRedFloatsWarp = 128;
 
@@ -697,9 +709,12 @@ rmsq_row_kernel(const Params p)
     float* nv_factor = WARP_ROWS ? red : red + 192;                         // [128]
     uint64_t* bars_all =
         reinterpret_cast<uint64_t*>(red + (WARP_ROWS ? kRedFloatsWarp : kRedFloats));  // [nrings][S]
-    // this thread's ring: its slots, its mbarriers, the thread that refills it, and its rows
+    long long* rows_all = reinterpret_cast<long long*>(bars_all + S * nrings);        // [nrings][S]
+    // this thread's ring: its slots, its mbarriers, the row of each slot (-1: the ring is done),
+    // the thread that refills it, and its rows
     unsigned char* ring = smem + (WARP_ROWS ? static_cast<size_t>(warp) * S * stage_bytes : 0);
     uint64_t* bars = bars_all + (WARP_ROWS ? warp * S : 0);
+    long long* slot_rows = rows_all + (WARP_ROWS ? warp * S : 0);
     const bool issuer = WARP_ROWS ? lane == 0 : tid == 0;
     const long long row0 = WARP_ROWS ? static_cast<long long>(blockIdx.x) * nwarps + warp
                                      : static_cast<long long>(blockIdx.x);
@@ -723,19 +738,70 @@ rmsq_row_kernel(const Params p)
     // visible, then let the next one start its own prologue while this grid runs.
     asm volatile("griddepcontrol.wait;" ::: "memory");
     asm volatile("griddepcontrol.launch_dependents;");
+    // The ring's rows, as its refilling thread hands them out: round-robin over the row
+    // processors below rows_static, then one at a time from the launch's counter; -1 when none
+    // is left. Counter tickets are taken one call ahead, so the atomic's round trip overlaps a
+    // whole row instead of delaying the refill. Each refilling thread stops at its first ticket
+    // past the last row, so the counter sees exactly (rows - rows_static) + (row processors)
+    // tickets; the thread holding the last of them is the last to touch it and sets it back to
+    // 0 for the counter's next launch.
+    long long next_static = row0;
+    unsigned int ahead = 0;       // counter ticket taken for the next call
+    bool have_ahead = false;
+    bool exhausted = false;
+    const unsigned long long last_ticket =
+        static_cast<unsigned long long>(p.rows - p.rows_static) + static_cast<unsigned long long>(rstep) - 1;
+    auto next_row = [&]() -> long long {
+        if (exhausted) return -1;
+        long long r;
+        if (next_static < p.rows_static) {
+            r = next_static;
+            next_static += rstep;
+            if (next_static >= p.rows_static && p.rowctr != nullptr) {
+                ahead = atomicAdd(p.rowctr, 1u);
+                have_ahead = true;
+            }
+        } else if (p.rowctr != nullptr) {
+            const unsigned int t = have_ahead ? ahead : atomicAdd(p.rowctr, 1u);
+            r = p.rows_static + static_cast<long long>(t);
+            have_ahead = false;
+            if (r >= p.rows) {
+                exhausted = true;
+                if (t == last_ticket) *p.rowctr = 0u;
+                return -1;
+            }
+            ahead = atomicAdd(p.rowctr, 1u);
+            have_ahead = true;
+        } else {
+            r = p.rows;
+        }
+        if (r >= p.rows) {
+            exhausted = true;
+            return -1;
+        }
+        return r;
+    };
+    // Give slot `st` (shared address `addr`) its next row: record the row number, then start the
+    // copies, or complete the slot's phase empty-handed when the ring has no row left. `reuse`:
+    // the slot's memory was read or written by threads before (order that before the copy).
+    auto refill = [&](int st, uint32_t addr, bool reuse) {
+        const long long r = next_row();
+        slot_rows[st] = r;
+        const uint32_t bar = smem_u32(&bars[st]);
+        if (r < 0) {
+            mbar_arrive(bar);
+            return;
+        }
+        if (reuse) fence_proxy_async_smem();
+        mbar_arrive_expect_tx(bar, stage_bytes);
+        bulk_load(addr, xg + r * nv, row_bytes, bar, policy);
+        if constexpr (RES) bulk_load(addr + row_bytes, rg + r * nv, row_bytes, bar, policy);
+    };
     if constexpr (RING) {
         // the ring's first rows, issued by the thread that initialised its barriers
-        if (issuer) {
-            for (int s = 0; s < S; ++s) {
-                const long long row = row0 + static_cast<long long>(s) * rstep;
-                if (row >= p.rows) break;
-                const uint32_t bar = smem_u32(&bars[s]);
-                const uint32_t dst = smem_u32(ring + static_cast<size_t>(s) * stage_bytes);
-                mbar_arrive_expect_tx(bar, stage_bytes);
-                bulk_load(dst, xg + row * nv, row_bytes, bar, policy);
-                if constexpr (RES) bulk_load(dst + row_bytes, rg + row * nv, row_bytes, bar, policy);
-            }
-        }
+        if (issuer)
+            for (int s = 0; s < S; ++s)
+                refill(s, smem_u32(ring + static_cast<size_t>(s) * stage_bytes), false);
     }
 
     float gs = 1.0f, gs_over_6 = 0.0f;
@@ -768,16 +834,30 @@ rmsq_row_kernel(const Params p)
     int stage = 0;          // ring slot of this row, and the mbarrier phase parity to wait for
     uint32_t parity = 0;
     int rbuf = 0;           // which of the two sum-of-squares reduction buffers this row uses
-    for (long long row = row0; row < p.rows; row += rstep) {
-        const uint4* __restrict__ xrow = xg + row * nv;
-        const uint4* __restrict__ rrow = RES ? rg + row * nv : nullptr;
-        // ---- load the row, add the residual, write residual_output, sum of squares ----------
+    bool aborted = false;   // a bounded wait ran out
+    long long reg_row = row0;
+    for (;;) {
+        // ---- which row: the slot's (ring schedules) or the next round-robin one --------------
         bool timed_out = false;
         uint32_t stage_addr = 0;
+        long long row;
         if constexpr (RING) {
             stage_addr = smem_u32(ring + static_cast<size_t>(stage) * stage_bytes);
             timed_out = !mbar_wait_bounded(smem_u32(&bars[stage]), parity, p.timeout_ns);
+            // The slot's row number was written before its barrier was armed, and an empty slot
+            // (-1) completes at once, so every thread of the ring reads the same value here.
+            row = slot_rows[stage];
+            if (row < 0) break;           // the ring handed out its last row
+        } else {
+            row = reg_row;
+            reg_row += rstep;
+            if (row >= p.rows) break;
         }
+        // false only after a timed-out wait; the loop then stops after the reduction's barrier
+        const bool have = !timed_out;
+        const uint4* __restrict__ xrow = xg + (have ? row : 0) * nv;
+        const uint4* __restrict__ rrow = RES ? rg + (have ? row : 0) * nv : nullptr;
+        // ---- load the row, add the residual, write residual_output, sum of squares ----------
         uint4 s[VPT];
         float2 acc_hi = make_float2(0.0f, 0.0f), acc_lo = make_float2(0.0f, 0.0f);
         float pmax = 0.0f;      // ONE_BAR: max |s w| over this thread's elements
@@ -785,7 +865,7 @@ rmsq_row_kernel(const Params p)
         for (int k = 0; k < VPT; ++k) {
             const int v = rt + k * RT;
             s[k] = make_uint4(0, 0, 0, 0);
-            if (v < nv && !timed_out) {
+            if (v < nv && have) {
                 uint4 xv, rv;
                 if constexpr (RING) {
                     xv = ld_shared_v4(stage_addr + v * 16u);
@@ -870,12 +950,10 @@ rmsq_row_kernel(const Params p)
             if constexpr (RING) {
                 if (issuer) {
                     atomicOr(p.err, ERRF_WAIT_TIMEOUT);
-                    // let the copies already issued for later rows land (bounded) before exit
+                    // let the copies already issued into the other slots land (bounded)
                     int js = stage;
                     uint32_t jp = parity;
                     for (int j = 1; j < S; ++j) {
-                        const long long jrow = row + static_cast<long long>(j) * rstep;
-                        if (jrow >= p.rows) break;
                         if (++js == S) {
                             js = 0;
                             jp ^= 1u;
@@ -884,21 +962,13 @@ rmsq_row_kernel(const Params p)
                     }
                 }
             }
-            return;
+            aborted = true;
+            break;
         }
         if constexpr (RING && !SMEM_S) {
-            // Every thread has read this slot (s is held in registers): refill it now with the
-            // row S iterations ahead.
+            // Every thread has read this slot (s is held in registers): refill it now.
             if constexpr (WARP_ROWS) __syncwarp();
-            const long long nrow = row + static_cast<long long>(S) * rstep;
-            if (issuer && nrow < p.rows) {
-                fence_proxy_async_smem();
-                const uint32_t bar = smem_u32(&bars[stage]);
-                mbar_arrive_expect_tx(bar, stage_bytes);
-                bulk_load(stage_addr, xg + nrow * nv, row_bytes, bar, policy);
-                if constexpr (RES)
-                    bulk_load(stage_addr + row_bytes, rg + nrow * nv, row_bytes, bar, policy);
-            }
+            if (issuer) refill(stage, stage_addr, true);
         }
         float rstd;
         if constexpr (WARP_ROWS) {
@@ -1209,15 +1279,7 @@ rmsq_row_kernel(const Params p)
             } else {
                 __syncthreads();
             }
-            const long long nrow = row + static_cast<long long>(S) * rstep;
-            if (issuer && nrow < p.rows) {
-                fence_proxy_async_smem();
-                const uint32_t bar = smem_u32(&bars[stage]);
-                mbar_arrive_expect_tx(bar, stage_bytes);
-                bulk_load(stage_addr, xg + nrow * nv, row_bytes, bar, policy);
-                if constexpr (RES)
-                    bulk_load(stage_addr + row_bytes, rg + nrow * nv, row_bytes, bar, policy);
-            }
+            if (issuer) refill(stage, stage_addr, true);
         }
         if constexpr (RING) {
             if (++stage == S) {
@@ -1226,6 +1288,7 @@ rmsq_row_kernel(const Params p)
             }
         }
     }
+    if (aborted) return;
     if constexpr (MODE == MODE_AMAX) {
         // non-negative floats order like their bit patterns, so an unsigned max is a float max
         run_max = warp_max(run_max);
