@@ -151,6 +151,30 @@ rmsq_status rmsnorm_nvfp4_global_scale(const void* input, const void* residual,
                                        float epsilon, float weight_offset, float* gs_out,
                                        void* stream);
 
+/* ---------------------------------------------------------------------------------------------
+ * rmsnorm_quant_fp8_static_scratch -- rmsnorm_quant_fp8 with its scratch in a fixed array.
+ * The pages have no counterpart: this is an addition for callers that cannot have a library
+ * allocate or hand out device memory on their behalf, for example a runtime that reserves all
+ * device memory itself before it starts serving, or a host thread that may not call the CUDA
+ * allocator. Arguments, layouts, results and errors are those of rmsnorm_quant_fp8 (bit for bit
+ * the same outputs), with these differences:
+ *   - The only scratch the kernel uses, the counter that hands out the last rows of a launch,
+ *     lives in a 256-byte array of this library's device memory, reserved on every GPU that
+ *     loads the library until the process exits. The call allocates and frees nothing.
+ *   - It clears that counter on `stream` before each launch. Every call shares the array, so
+ *     calls that overlap on the GPU (other streams, other host threads) race and can hand out
+ *     rows twice or not at all; order them on one stream.
+ *   - rows above 2^31 - 1 (what the 32-bit counter can hand out) return RMSQ_ERR_SHAPE.
+ *   - The first call on a device looks up the array's device address (cudaGetSymbolAddress) and
+ *     returns RMSQ_ERR_DEVICE if that fails; make that first call before any stream capture.
+ * ------------------------------------------------------------------------------------------- */
+rmsq_status rmsnorm_quant_fp8_static_scratch(const void* input, const void* residual,
+                                             void* residual_output, const void* gamma,
+                                             int64_t rows, int64_t hidden, int dtype,
+                                             float epsilon, float weight_offset, float scale_ub,
+                                             void* output, void* scale_output, int scale_dtype,
+                                             void* stream);
+
 /* Human-readable name of a status code (static storage; never NULL). */
 const char* rmsq_status_string(rmsq_status status);
 

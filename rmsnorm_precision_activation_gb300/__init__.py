@@ -35,6 +35,7 @@ _DT = {torch.bfloat16: RMSQ_BF16, torch.float16: RMSQ_FP16, torch.float32: RMSQ_
 _P, _I64, _I, _F, _U64 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_float, ctypes.c_uint64
 SIGNATURES = {
     "rmsnorm_quant_fp8": ([_P, _P, _P, _P, _I64, _I64, _I, _F, _F, _F, _P, _P, _I, _P], _I),
+    "rmsnorm_quant_fp8_static_scratch": ([_P, _P, _P, _P, _I64, _I64, _I, _F, _F, _F, _P, _P, _I, _P], _I),
     "rmsnorm_quant_nvfp4": ([_P, _P, _P, _P, _I64, _I64, _I, _F, _F, _P, _P, _P, _I, _P], _I),
     "rmsnorm_quant_mxfp4": ([_P, _P, _P, _P, _I64, _I64, _I, _F, _F, _P, _P, _I, _P], _I),
     "rmsnorm_nvfp4_global_scale": ([_P, _P, _P, _I64, _I64, _I, _F, _F, _P, _P], _I),

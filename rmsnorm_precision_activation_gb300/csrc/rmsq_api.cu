@@ -1,6 +1,7 @@
 // rmsq_api.cu -- the C ABI of librmsq.so: argument checks, launch planning, the entry points
 // declared in include/rmsq.h, and a few small diagnostic kernels.
 #include <atomic>
+#include <climits>
 #include <cmath>
 #include <cstdint>
 #include <cstring>
@@ -138,8 +139,13 @@ cudaError_t run_kernel(const void* fn, const Plan& pl, const Params& p, cudaStre
     q.rows_static = p.rows;
     if (g_dynamic_rows.load() && pl.sched == SCHED_PIPE && di.counters != nullptr && p.rows >= 2 * procs &&
         p.rows < (1LL << 31)) {
-        const unsigned long long slot = g_counter_seq.fetch_add(1) % kCounterSlots;
-        q.rowctr = di.counters + slot * 8;
+        // a counter the caller set up (zeroed, on this stream) is used as it is
+        if (p.rowctr != nullptr) {
+            q.rowctr = p.rowctr;
+        } else {
+            const unsigned long long slot = g_counter_seq.fetch_add(1) % kCounterSlots;
+            q.rowctr = di.counters + slot * 8;
+        }
         q.rows_static = p.rows / procs * 3 / 4 * procs;
     }
     void* args[] = {&q};
@@ -407,6 +413,72 @@ extern "C" rmsq_status rmsnorm_quant_fp8(const void* input, const void* residual
     p.scale_ub = scale_ub;
     p.scale_dtype = scale_dtype;
     return launch(MODE_FP8, p, residual != nullptr, dtype, *di, static_cast<cudaStream_t>(stream));
+}
+
+// ------------------------------------------------------------------------------------------
+// rmsnorm_quant_fp8_static_scratch: the FP8 call with its scratch in a file-scope array
+// ------------------------------------------------------------------------------------------
+
+// The FP8 kernel's only scratch is the 32-bit counter that hands out the last rows of a launch.
+// For callers that must know every byte of device memory the library touches, this entry point
+// keeps that counter in its own 256-byte array, reserved on every device that loads the library
+// until the process exits, and clears it on the caller's stream before each launch.
+constexpr int kStaticScratchWords = 64;
+static __device__ __align__(256) unsigned int g_fp8_static_scratch[kStaticScratchWords];
+static unsigned int* g_fp8_static_scratch_addr[kMaxDevices];   // its device address, per device
+
+extern "C" rmsq_status rmsnorm_quant_fp8_static_scratch(
+    const void* input, const void* residual, void* residual_output, const void* gamma,
+    int64_t rows, int64_t hidden, int dtype, float epsilon, float weight_offset, float scale_ub,
+    void* output, void* scale_output, int scale_dtype, void* stream)
+{
+    bool empty;
+    rmsq_status st = check_common(input, residual, residual_output, gamma, rows, hidden, dtype,
+                                  epsilon, weight_offset, dtype == RMSQ_F32 ? 4 : 8, &empty);
+    if (st != RMSQ_OK) return st;
+    if (scale_dtype != RMSQ_F32 && scale_dtype != RMSQ_BF16 && scale_dtype != RMSQ_FP16)
+        return RMSQ_ERR_DTYPE;
+    if (!(scale_ub > 0.0f)) return RMSQ_ERR_VALUE;
+    if (rows > INT32_MAX) return RMSQ_ERR_SHAPE;   // beyond what the 32-bit counter can hand out
+    if (empty) return RMSQ_OK;
+    if (!output || !scale_output) return RMSQ_ERR_NULL;
+    if (!aligned16(output) || !aligned16(scale_output)) return RMSQ_ERR_ALIGN;
+    const DeviceInfo* di = device_info();
+    if (!di) return RMSQ_ERR_DEVICE;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return RMSQ_ERR_DEVICE;
+    }
+    unsigned int* scratch = nullptr;
+    {
+        // first call on this device: look up the array's device address (the name alone is a
+        // host-side stand-in, not an address a kernel can use)
+        std::lock_guard<std::mutex> lock(g_mu);
+        if (g_fp8_static_scratch_addr[dev] == nullptr) {
+            void* addr = nullptr;
+            if (cudaGetSymbolAddress(&addr, g_fp8_static_scratch) != cudaSuccess || addr == nullptr) {
+                cudaGetLastError();
+                return RMSQ_ERR_DEVICE;
+            }
+            g_fp8_static_scratch_addr[dev] = static_cast<unsigned int*>(addr);
+        }
+        scratch = g_fp8_static_scratch_addr[dev];
+    }
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    // the counter must start at zero; the last call may have left anything in it
+    if (cudaMemsetAsync(scratch, 0, sizeof(unsigned int) * kStaticScratchWords, s) != cudaSuccess) {
+        cudaGetLastError();
+        return RMSQ_ERR_LAUNCH;
+    }
+    Params p = base_params(input, residual, residual_output, gamma, rows, hidden, dtype, epsilon,
+                           weight_offset, *di);
+    p.out = output;
+    p.scale_out = scale_output;
+    p.scale_ub = scale_ub;
+    p.scale_dtype = scale_dtype;
+    p.rowctr = scratch;
+    return launch(MODE_FP8, p, residual != nullptr, dtype, *di, s);
 }
 
 static rmsq_status fp4_common(int mode, const void* input, const void* residual,
