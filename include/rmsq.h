@@ -73,7 +73,8 @@ typedef enum {
                              residual_output is given */
     RMSQ_ERR_SHAPE = 2,   /* rows < 0, or hidden outside [block, RMSQ_MAX_HIDDEN] or not a
                              multiple of the mode's block (FP8: 8 elements for 16-bit types and
-                             4 for fp32; NVFP4: 16; MXFP4: 32) */
+                             4 for fp32; NVFP4: 16; MXFP4: 32), or a row wider than
+                             RMSQ_ONE_CTA_HIDDEN that is not a multiple of 256 elements */
     RMSQ_ERR_ALIGN = 3,   /* a data pointer is not 16-byte aligned */
     RMSQ_ERR_DTYPE = 4,   /* unknown rmsq_dtype, scale dtype or scale layout */
     RMSQ_ERR_LAUNCH = 5,  /* the CUDA launch failed (cudaGetLastError after launch) */
@@ -83,8 +84,11 @@ typedef enum {
     RMSQ_ERR_TIMEOUT = 8  /* reported by rmsq_device_status: a bounded device-side wait ran out */
 } rmsq_status;
 
-/* Largest hidden size any entry point accepts, in elements (fp32 input: half of it). */
-#define RMSQ_MAX_HIDDEN 32768
+/* Largest hidden size any entry point accepts, in elements (fp32 input: half of it). Rows wider
+ * than RMSQ_ONE_CTA_HIDDEN (fp32: half of it) are split over a thread-block cluster of up to 16
+ * CTAs and must be a multiple of 256 elements. */
+#define RMSQ_MAX_HIDDEN 131072
+#define RMSQ_ONE_CTA_HIDDEN 32768
 
 /* ---------------------------------------------------------------------------------------------
  * rmsnorm_quant_fp8 -- residual add + RMSNorm + FP8 E4M3 with a per-row dynamic scale.
@@ -194,8 +198,10 @@ rmsq_status rmsq_device_status(void);
  *                    1 = bulk-copy pipeline (rows staged in shared memory by the TMA engine, a
  *                    CTA per row), 2 = register-staged rows, 3 = row per warp (each warp owns
  *                    whole rows with its own bulk-copy ring; rows up to 256 vectors of 16 bytes,
- *                    i.e. hidden <= 2048 for 16-bit input). Returns the previous value. A forced
- *                    schedule that does not fit the row falls back to 1, and 1 to 2.
+ *                    i.e. hidden <= 2048 for 16-bit input), 4 = a thread-block cluster per row
+ *                    (each CTA takes a slice through its own ring; the slices' sums meet in
+ *                    distributed shared memory). Returns the previous value. A forced schedule
+ *                    that does not fit the row falls back to the automatic choice.
  * rmsq_set_tuning    overrides the pipeline depth (stages, 0 = automatic), CTAs per SM
  *                    (0 = automatic) and vectors of 16 bytes per thread per row (0 = automatic;
  *                    1, 2, 4 or 8). Returns RMSQ_ERR_VALUE for values out of range; a setting
@@ -203,6 +209,9 @@ rmsq_status rmsq_device_status(void);
  *                    RMSQ_ERR_SHAPE.
  * rmsq_set_row_warps  warps per CTA of the row-per-warp schedule (0 = automatic, at most 16).
  *                    Returns RMSQ_ERR_VALUE out of range.
+ * rmsq_set_cluster_size  CTAs per cluster of the cluster schedule (0 = automatic, else 2, 4, 8
+ *                    or 16); the schedule itself is forced with rmsq_set_schedule(4). Returns
+ *                    RMSQ_ERR_VALUE for other values.
  * rmsq_set_dynamic_rows  the CTA-per-row schedule hands the last quarter of its rows out one at a
  *                    time from a per-launch counter in the library's device memory, so CTAs on
  *                    SMs that get more HBM bandwidth take more rows (default). 0 deals every row
@@ -222,6 +231,7 @@ rmsq_status rmsq_device_status(void);
 int rmsq_set_schedule(int schedule);
 rmsq_status rmsq_set_tuning(int stages, int ctas_per_sm, int vectors_per_thread);
 rmsq_status rmsq_set_row_warps(int warps_per_cta);
+rmsq_status rmsq_set_cluster_size(int ctas_per_cluster);
 int rmsq_set_dynamic_rows(int enable);
 int rmsq_set_pdl(int enable);
 void rmsq_set_wait_timeout_ns(uint64_t timeout_ns);

@@ -22,7 +22,7 @@ LIB_PATH = os.path.join(_HERE, "librmsq.so")
 
 RMSQ_BF16, RMSQ_FP16, RMSQ_F32 = 0, 1, 2
 SCALE_ROW_MAJOR, SCALE_SWIZZLED_128x4 = 0, 1
-SCHED_AUTO, SCHED_PIPE, SCHED_REG, SCHED_WARP = 0, 1, 2, 3
+SCHED_AUTO, SCHED_PIPE, SCHED_REG, SCHED_WARP, SCHED_CLUSTER = 0, 1, 2, 3, 4
 MAX_HIDDEN = 32768
 
 STATUS = {0: "RMSQ_OK", 1: "RMSQ_ERR_NULL", 2: "RMSQ_ERR_SHAPE", 3: "RMSQ_ERR_ALIGN",
@@ -44,6 +44,7 @@ SIGNATURES = {
     "rmsq_set_schedule": ([_I], _I),
     "rmsq_set_tuning": ([_I, _I, _I], _I),
     "rmsq_set_row_warps": ([_I], _I),
+    "rmsq_set_cluster_size": ([_I], _I),
     "rmsq_set_dynamic_rows": ([_I], _I),
     "rmsq_set_pdl": ([_I], _I),
     "rmsq_set_wait_timeout_ns": ([_U64], None),
@@ -232,6 +233,10 @@ def rmsq_set_schedule(schedule: int) -> int:
 
 def rmsq_set_tuning(stages: int = 0, ctas_per_sm: int = 0, vectors_per_thread: int = 0):
     _check(lib().rmsq_set_tuning(stages, ctas_per_sm, vectors_per_thread), "rmsq_set_tuning")
+
+
+def rmsq_set_cluster_size(ctas_per_cluster: int = 0):
+    _check(lib().rmsq_set_cluster_size(int(ctas_per_cluster)), "rmsq_set_cluster_size")
 
 
 def rmsq_set_row_warps(warps_per_cta: int = 0):

@@ -31,6 +31,7 @@ static std::atomic<int> g_tune_stages{0};
 static std::atomic<int> g_tune_ctas{0};
 static std::atomic<int> g_tune_vpt{0};
 static std::atomic<int> g_tune_warps{0};
+static std::atomic<int> g_tune_cluster{0};
 static std::atomic<unsigned long long> g_timeout_ns{2000000000ull};
 static std::atomic<unsigned long long> g_launches{0};
 static std::atomic<bool> g_pdl{true};
@@ -84,7 +85,7 @@ static const DeviceInfo* device_info()
 
 struct OccEntry {
     const void* fn;
-    int dev, threads, smem, blocks;
+    int dev, threads, smem, cluster, blocks;   // blocks: per SM, or active clusters (cluster > 1)
     bool attr_set;
 };
 static OccEntry g_occ[512];
@@ -99,9 +100,10 @@ cudaError_t run_kernel(const void* fn, const Plan& pl, const Params& p, cudaStre
     {
         std::lock_guard<std::mutex> lock(g_mu);
         int i = 0;
+        const int cl = pl.sched == SCHED_CLUSTER ? pl.cluster : 1;
         for (; i < g_nocc; ++i)
             if (g_occ[i].fn == fn && g_occ[i].dev == dev && g_occ[i].threads == pl.threads &&
-                g_occ[i].smem == pl.smem)
+                g_occ[i].smem == pl.smem && g_occ[i].cluster == cl)
                 break;
         if (i == g_nocc) {
             cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -112,21 +114,49 @@ cudaError_t run_kernel(const void* fn, const Plan& pl, const Params& p, cudaStre
             e = cudaFuncSetAttribute(fn, cudaFuncAttributePreferredSharedMemoryCarveout,
                                      cudaSharedmemCarveoutMaxShared);
             if (e != cudaSuccess) return e;
+            if (cl > 8) {
+                // clusters of 16 CTAs are beyond the portable size of 8
+                e = cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+                if (e != cudaSuccess) return e;
+            }
             int b = 0;
-            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, fn, pl.threads, pl.smem);
+            if (cl > 1) {
+                // how many clusters of cl CTAs can be resident at once
+                cudaLaunchConfig_t oc = {};
+                oc.gridDim = dim3(static_cast<unsigned>(cl));
+                oc.blockDim = dim3(pl.threads);
+                oc.dynamicSmemBytes = static_cast<size_t>(pl.smem);
+                cudaLaunchAttribute ca[1];
+                ca[0].id = cudaLaunchAttributeClusterDimension;
+                ca[0].val.clusterDim.x = static_cast<unsigned>(cl);
+                ca[0].val.clusterDim.y = 1;
+                ca[0].val.clusterDim.z = 1;
+                oc.attrs = ca;
+                oc.numAttrs = 1;
+                e = cudaOccupancyMaxActiveClusters(&b, fn, &oc);
+            } else {
+                e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, fn, pl.threads, pl.smem);
+            }
             if (e != cudaSuccess) return e;
             if (g_nocc < static_cast<int>(sizeof(g_occ) / sizeof(g_occ[0])))
-                g_occ[g_nocc++] = OccEntry{fn, dev, pl.threads, pl.smem, b, true};
+                g_occ[g_nocc++] = OccEntry{fn, dev, pl.threads, pl.smem, cl, b, true};
             blocks = b;
         } else {
             blocks = g_occ[i].blocks;
         }
     }
     if (blocks < 1) return cudaErrorInvalidConfiguration;
-    if (pl.ctas_per_sm > 0 && blocks > pl.ctas_per_sm) blocks = pl.ctas_per_sm;
-    long long grid = static_cast<long long>(blocks) * di.sms;
+    long long grid;
+    if (pl.sched == SCHED_CLUSTER) {
+        // one cluster per row at a time; as many clusters as can be resident, at most one per row
+        const long long clusters = p.rows < blocks ? p.rows : blocks;
+        grid = clusters * pl.cluster;
+    } else {
+        if (pl.ctas_per_sm > 0 && blocks > pl.ctas_per_sm) blocks = pl.ctas_per_sm;
+        grid = static_cast<long long>(blocks) * di.sms;
+    }
     const long long rows_per_cta = pl.sched == SCHED_WARP ? pl.threads / 32 : 1;
-    if (grid > (p.rows + rows_per_cta - 1) / rows_per_cta)
+    if (pl.sched != SCHED_CLUSTER && grid > (p.rows + rows_per_cta - 1) / rows_per_cta)
         grid = (p.rows + rows_per_cta - 1) / rows_per_cta;
     // Dynamic row tail (CTA-per-row ring schedule): SMs do not get equal shares of HBM
     // bandwidth, so with rows dealt out round-robin the slowest SM sets the end of the launch
@@ -156,11 +186,18 @@ cudaError_t run_kernel(const void* fn, const Plan& pl, const Params& p, cudaStre
     cfg.blockDim = dim3(pl.threads);
     cfg.dynamicSmemBytes = static_cast<size_t>(pl.smem);
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = g_pdl.load() ? 1 : 0;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
+    if (pl.sched == SCHED_CLUSTER) {
+        attr[1].id = cudaLaunchAttributeClusterDimension;
+        attr[1].val.clusterDim.x = static_cast<unsigned>(pl.cluster);
+        attr[1].val.clusterDim.y = 1;
+        attr[1].val.clusterDim.z = 1;
+        cfg.numAttrs = 2;
+    }
     cudaError_t e = cudaLaunchKernelExC(&cfg, fn, args);
     if (e == cudaSuccess) g_launches.fetch_add(1, std::memory_order_relaxed);
     return e;
@@ -225,6 +262,48 @@ static bool make_plan(int mode, int dt, bool res, bool w16, int hidden, const De
         return true;
     }
 
+    // A cluster of C CTAs per row: for rows whose two-slot ring does not fit one CTA's shared
+    // memory (or when forced). The smallest C of 2, 4, 8, 16 whose slice slot holds at most 32 KB
+    // (three CTAs per SM, so one CTA's row-end barrier and exchange overlap the others' work;
+    // measured on GB300: 4.5-5.1 TB/s against 3.7-4.5 TB/s with one CTA per SM at 32768), else
+    // the smallest whose ring fits; slices hold whole FP4 scale blocks; 4 or 8 vectors per
+    // thread, at most 256 threads.
+    const int red_bytes = kRedFloats * 4;
+    const bool pipe_fits = 2 * stage + red_bytes + 2 * 16 <= di.smem_optin;
+    if (forced == SCHED_CLUSTER || (!pipe_fits && forced != SCHED_REG)) {
+        const int tune_c = g_tune_cluster.load();
+        const int blk = mode == MODE_MXFP4 ? 32 : 16;
+        int best = 0;
+        for (int c = 2; c <= 16; c *= 2) {
+            if (tune_c != 0 && c != tune_c) continue;
+            if (nv % c != 0) continue;
+            const int nvc = nv / c;
+            if (mode != MODE_FP8 && (nvc * elems_per_vec(dt)) % blk != 0) continue;
+            const long long cstage = static_cast<long long>(nvc) * 16 * (res ? 2 : 1);
+            if (2 * cstage + red_bytes + 2 * 16 + kClusterXchBytes > di.smem_optin) continue;
+            if ((nvc + 7) / 8 > 512) continue;
+            if (best == 0) best = c;              // smallest that fits
+            if (cstage <= 32768 || tune_c != 0) {
+                best = c;                         // smallest with a small slot
+                break;
+            }
+        }
+        if (best != 0) {
+            const int nvc = nv / best;
+            const long long cstage = static_cast<long long>(nvc) * 16 * (res ? 2 : 1);
+            int cv = 4;
+            while (cv < 8 && nvc > 256 * cv) cv *= 2;
+            pl.sched = SCHED_CLUSTER;
+            pl.cluster = best;
+            pl.vpt = cv;
+            pl.threads = ((nvc + cv - 1) / cv + 31) / 32 * 32;
+            pl.stages = 2;
+            pl.smem = static_cast<int>(2 * cstage + red_bytes + 2 * 16 + kClusterXchBytes);
+            pl.ctas_per_sm = 0;
+            return true;
+        }
+    }
+
     int vpt = g_tune_vpt.load();
     if (vpt == 0) {
         if (mode != MODE_FP8 && mode != MODE_AMAX && res) {
@@ -249,8 +328,6 @@ static bool make_plan(int mode, int dt, bool res, bool w16, int hidden, const De
     pl.vpt = vpt;
     pl.threads = threads;
 
-    const int red_bytes = kRedFloats * 4;
-    const bool pipe_fits = 2 * stage + red_bytes + 2 * 16 <= di.smem_optin;
     pl.sched = (forced == SCHED_REG || !pipe_fits) ? SCHED_REG : SCHED_PIPE;
     pl.ctas_per_sm = g_tune_ctas.load();
     if (pl.ctas_per_sm == 0) {
@@ -284,8 +361,10 @@ static rmsq_status check_common(const void* input, const void* residual, const v
     *empty = false;
     if (dtype != RMSQ_BF16 && dtype != RMSQ_FP16 && dtype != RMSQ_F32) return RMSQ_ERR_DTYPE;
     const int64_t max_h = dtype == RMSQ_F32 ? RMSQ_MAX_HIDDEN / 2 : RMSQ_MAX_HIDDEN;
+    const int64_t one_cta = dtype == RMSQ_F32 ? RMSQ_ONE_CTA_HIDDEN / 2 : RMSQ_ONE_CTA_HIDDEN;
     if (rows < 0 || hidden < min_multiple || hidden > max_h || hidden % min_multiple != 0)
         return RMSQ_ERR_SHAPE;
+    if (hidden > one_cta && hidden % 256 != 0) return RMSQ_ERR_SHAPE;   // cluster slices
     if (!(epsilon >= 0.0f) || !std::isfinite(epsilon) || !std::isfinite(weight_offset))
         return RMSQ_ERR_VALUE;
     if (rows == 0) {
@@ -606,7 +685,7 @@ extern "C" rmsq_status rmsq_device_status(void)
 
 extern "C" int rmsq_set_schedule(int schedule)
 {
-    if (schedule < 0 || schedule > 3) schedule = 0;
+    if (schedule < 0 || schedule > 4) schedule = 0;
     return g_schedule.exchange(schedule);
 }
 
@@ -626,6 +705,15 @@ extern "C" rmsq_status rmsq_set_row_warps(int warps_per_cta)
 {
     if (warps_per_cta < 0 || warps_per_cta > 16) return RMSQ_ERR_VALUE;
     g_tune_warps = warps_per_cta;
+    return RMSQ_OK;
+}
+
+extern "C" rmsq_status rmsq_set_cluster_size(int ctas_per_cluster)
+{
+    if (ctas_per_cluster != 0 && ctas_per_cluster != 2 && ctas_per_cluster != 4 &&
+        ctas_per_cluster != 8 && ctas_per_cluster != 16)
+        return RMSQ_ERR_VALUE;
+    g_tune_cluster = ctas_per_cluster;
     return RMSQ_OK;
 }
 

@@ -16,6 +16,11 @@
 //   SCHED_WARP  row per warp, for short rows: every warp of a CTA owns whole rows with its own
 //               ring of row buffers and mbarriers (lane 0 issues the bulk copies), and all
 //               reductions are warp shuffles -- no CTA barrier and no cross-warp stage per row.
+//   SCHED_CLUSTER  rows wider than one CTA's ring holds: a thread-block cluster of C CTAs
+//               shares each row, CTA k taking the k-th 1/C of it through its own ring. The
+//               CTAs' row sums (and maxima) meet in distributed shared memory: each CTA writes
+//               its partial into its own exchange slot, one cluster barrier, then every CTA
+//               reads all C slots in rank order, so every CTA forms the same totals.
 //
 // Method sources: Modular Mojo API docs "rms_norm_fused_fp8" / "allreduce_residual_rmsnorm_fp8"
 // (FP8 row scale with scale_ub, residual_output, weight_offset on gamma) and FlashInfer
@@ -31,7 +36,7 @@ namespace rmsq {
 enum { DT_BF16 = 0, DT_FP16 = 1, DT_F32 = 2 };
 // MODE_AMAX is the NVFP4 global-scale pre-pass: y is formed but only max |y| leaves the kernel.
 enum { MODE_FP8 = 0, MODE_NVFP4 = 1, MODE_MXFP4 = 2, MODE_AMAX = 3 };
-enum { SCHED_PIPE = 1, SCHED_REG = 2, SCHED_WARP = 3 };
+enum { SCHED_PIPE = 1, SCHED_REG = 2, SCHED_WARP = 3, SCHED_CLUSTER = 4 };
 
 // Error flag bits set on the device.
 enum { ERRF_WAIT_TIMEOUT = 1u };
@@ -113,6 +118,55 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
         : "r"(bar), "r"(parity)
         : "memory");
     return done != 0;
+}
+
+// Thread-block cluster: this CTA's rank, the cluster size, this cluster's index and the count.
+__device__ __forceinline__ uint32_t cluster_rank()
+{
+    uint32_t r;
+    asm("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t cluster_size()
+{
+    uint32_t r;
+    asm("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t cluster_id()
+{
+    uint32_t r;
+    asm("mov.u32 %0, %%clusterid.x;" : "=r"(r));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t cluster_count()
+{
+    uint32_t r;
+    asm("mov.u32 %0, %%nclusterid.x;" : "=r"(r));
+    return r;
+}
+
+// Every thread of every CTA of the cluster: shared-memory writes before it are visible to the
+// cluster's reads after it.
+__device__ __forceinline__ void cluster_sync()
+{
+    asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
+}
+
+// Read a float4 at shared address `addr` of the CTA with cluster rank `rank`.
+__device__ __forceinline__ float4 ld_cluster_f4(uint32_t addr, uint32_t rank)
+{
+    uint32_t raddr;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(raddr) : "r"(addr), "r"(rank));
+    float4 v;
+    asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "r"(raddr)
+                 : "memory");
+    return v;
 }
 
 __device__ __forceinline__ unsigned long long globaltimer_ns()
@@ -647,9 +701,11 @@ struct GammaRegs<E, VPT, false> {
 // Shared memory after the stage rings: [2][32] float2 sum-of-squares partials, [2][32] row
 // maxima, [128] NVFP4 element factors gs / dec(s) indexed by the E4M3 block-scale code (the
 // row-per-warp schedule reduces in registers and keeps only the factor table), then per ring
-// [stages] mbarriers and [stages] row numbers of the slots.
+// [stages] mbarriers and [stages] row numbers of the slots, then (SCHED_CLUSTER) the cluster
+// exchange slots: [2] float4 {sum hi, sum lo, max, stop} and [2] float4 {amax, -, -, -}.
 constexpr int kRedFloats = 2 * 32 * 2 + 2 * 32 + 128;
 constexpr int kRedFloatsWarp = 128;
+constexpr int kClusterXchBytes = 4 * 16;
 
 // ------------------------------------------------------------------------------------------
 // The kernel
@@ -675,7 +731,8 @@ rmsq_row_kernel(const Params p)
     // SCHED_WARP: every warp is its own row processor (rows, ring and mbarriers per warp); the
     // bulk-copy ring logic is shared with SCHED_PIPE.
     constexpr bool WARP_ROWS = SCHED == SCHED_WARP;
-    constexpr bool RING = SCHED == SCHED_PIPE || WARP_ROWS;
+    constexpr bool CLUSTER = SCHED == SCHED_CLUSTER;
+    constexpr bool RING = SCHED == SCHED_PIPE || WARP_ROWS || CLUSTER;
     // The ring schedules can keep the row in its shared-memory slot until the row is done: pass 1 writes
     // the residual sum s back over x and later passes re-read it, so no row data is held in
     // registers across the CTA barrier (the slot is refilled after an end-of-row barrier). That
@@ -697,7 +754,12 @@ rmsq_row_kernel(const Params p)
     const int nwarps = T >> 5;
     const int rt = WARP_ROWS ? lane : tid;       // this thread's index within its row
     const int RT = WARP_ROWS ? 32 : T;           // threads per row
-    const int nv = p.nvec;
+    // SCHED_CLUSTER: this CTA's slice of every row is vectors [voff, voff + nv) of stride
+    const uint32_t crank = CLUSTER ? cluster_rank() : 0u;
+    const uint32_t csize = CLUSTER ? cluster_size() : 1u;
+    const int nv = CLUSTER ? p.nvec / static_cast<int>(csize) : p.nvec;   // vectors handled
+    const long long stride = p.nvec;                                      // vectors per row
+    const int voff = static_cast<int>(crank) * nv;
     const uint32_t row_bytes = static_cast<uint32_t>(nv) * 16u;
     const uint32_t stage_bytes = row_bytes * (RES ? 2u : 1u);
     const int S = RING ? p.stages : 0;
@@ -715,15 +777,20 @@ rmsq_row_kernel(const Params p)
     unsigned char* ring = smem + (WARP_ROWS ? static_cast<size_t>(warp) * S * stage_bytes : 0);
     uint64_t* bars = bars_all + (WARP_ROWS ? warp * S : 0);
     long long* slot_rows = rows_all + (WARP_ROWS ? warp * S : 0);
+    float4* xch = reinterpret_cast<float4*>(rows_all + S * nrings);                  // [4]
     const bool issuer = WARP_ROWS ? lane == 0 : tid == 0;
     const long long row0 = WARP_ROWS ? static_cast<long long>(blockIdx.x) * nwarps + warp
+                           : CLUSTER ? static_cast<long long>(cluster_id())
                                      : static_cast<long long>(blockIdx.x);
     const long long rstep = WARP_ROWS ? static_cast<long long>(gridDim.x) * nwarps
+                            : CLUSTER ? static_cast<long long>(cluster_count())
                                       : static_cast<long long>(gridDim.x);
 
-    const uint4* __restrict__ xg = static_cast<const uint4*>(p.x);
-    const uint4* __restrict__ rg = static_cast<const uint4*>(p.res);
-    uint4* __restrict__ rog = static_cast<uint4*>(p.res_out);
+    const uint4* __restrict__ xg = static_cast<const uint4*>(p.x) + voff;
+    const uint4* __restrict__ rg = RES ? static_cast<const uint4*>(p.res) + voff : nullptr;
+    uint4* __restrict__ rog = RES ? static_cast<uint4*>(p.res_out) + voff : nullptr;
+    // first block scale of this CTA's slice (FP4), and the byte offset of its codes
+    const int sf_off = voff * EPV / BLOCK;
 
     uint64_t policy = 0;
     if constexpr (RING) {
@@ -794,8 +861,8 @@ rmsq_row_kernel(const Params p)
         }
         if (reuse) fence_proxy_async_smem();
         mbar_arrive_expect_tx(bar, stage_bytes);
-        bulk_load(addr, xg + r * nv, row_bytes, bar, policy);
-        if constexpr (RES) bulk_load(addr + row_bytes, rg + r * nv, row_bytes, bar, policy);
+        bulk_load(addr, xg + r * stride, row_bytes, bar, policy);
+        if constexpr (RES) bulk_load(addr + row_bytes, rg + r * stride, row_bytes, bar, policy);
     };
     if constexpr (RING) {
         // the ring's first rows, issued by the thread that initialised its barriers
@@ -819,7 +886,7 @@ rmsq_row_kernel(const Params p)
 
     const float2 offset2 = splat(p.offset);
     GammaRegs<E, VPT, !W16 && VPT <= 4> G;
-    G.load(static_cast<const uint4*>(p.gamma), rt, RT, nv, offset2, NV_BLOCKED ? GROUP : 1);
+    G.load(static_cast<const uint4*>(p.gamma) + voff, rt, RT, nv, offset2, NV_BLOCKED ? GROUP : 1);
     constexpr bool sw_exact = W16;                            // s * gamma exact in fp32
     const float Hf = static_cast<float>(p.hidden);
     // lanes in the second reduction stage: the smallest power of two >= nwarps
@@ -835,6 +902,8 @@ rmsq_row_kernel(const Params p)
     uint32_t parity = 0;
     int rbuf = 0;           // which of the two sum-of-squares reduction buffers this row uses
     bool aborted = false;   // a bounded wait ran out
+    int cpar = 0;           // SCHED_CLUSTER: which of the two sum exchange slots this row uses
+    int mpar = 0;           // SCHED_CLUSTER: the same for the FP8 row amax
     long long reg_row = row0;
     for (;;) {
         // ---- which row: the slot's (ring schedules) or the next round-robin one --------------
@@ -855,8 +924,8 @@ rmsq_row_kernel(const Params p)
         }
         // false only after a timed-out wait; the loop then stops after the reduction's barrier
         const bool have = !timed_out;
-        const uint4* __restrict__ xrow = xg + (have ? row : 0) * nv;
-        const uint4* __restrict__ rrow = RES ? rg + (have ? row : 0) * nv : nullptr;
+        const uint4* __restrict__ xrow = xg + row * stride;
+        const uint4* __restrict__ rrow = RES ? rg + row * stride : nullptr;
         // ---- load the row, add the residual, write residual_output, sum of squares ----------
         uint4 s[VPT];
         float2 acc_hi = make_float2(0.0f, 0.0f), acc_lo = make_float2(0.0f, 0.0f);
@@ -876,7 +945,7 @@ rmsq_row_kernel(const Params p)
                 }
                 if constexpr (RES) {
                     s[k] = E::add(xv, rv);
-                    if constexpr (MODE != MODE_AMAX) st_v4(rog + row * nv + v, s[k]);
+                    if constexpr (MODE != MODE_AMAX) st_v4(rog + row * stride + v, s[k]);
                     if constexpr (SMEM_S) st_shared_v4(stage_addr + v * 16u, s[k]);
                 } else {
                     s[k] = xv;
@@ -946,6 +1015,56 @@ rmsq_row_kernel(const Params p)
         bool stop;
         if constexpr (WARP_ROWS) stop = __any_sync(0xFFFFFFFFu, timed_out);
         else stop = __syncthreads_or(timed_out);
+        // the row's (or, for SCHED_CLUSTER, this CTA's slice's) sum of squares and ONE_BAR max,
+        // the same in every thread
+        FF tot = ss;
+        float tmax = pmax;
+        if constexpr (!WARP_ROWS) {
+            const float2 part = lane < nwarps ? red_ss[lane] : make_float2(0.0f, 0.0f);
+            if constexpr (EXACT) {
+                FF t{part.x, part.y};
+#pragma unroll
+                for (int o = 8; o > 0; o >>= 1)
+                    if (o < red_lanes) t = ff_add(t, shfl_xor_ff(t, o));
+                tot.hi = __shfl_sync(0xFFFFFFFFu, t.hi, 0);
+                tot.lo = __shfl_sync(0xFFFFFFFFu, t.lo, 0);
+                if constexpr (ONE_BAR) {
+                    float m = lane < nwarps ? red_max[lane] : 0.0f;
+#pragma unroll
+                    for (int o = 8; o > 0; o >>= 1)
+                        if (o < red_lanes) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+                    tmax = __shfl_sync(0xFFFFFFFFu, m, 0);
+                }
+            } else {
+                float t = part.x;
+#pragma unroll
+                for (int o = 8; o > 0; o >>= 1)
+                    if (o < red_lanes) t += __shfl_xor_sync(0xFFFFFFFFu, t, o);
+                tot = FF{__shfl_sync(0xFFFFFFFFu, t, 0), 0.0f};
+            }
+        }
+        if constexpr (CLUSTER) {
+            // The cluster's CTAs trade their slice totals (and whether any wait ran out): each
+            // writes its own slot, one cluster barrier, then every CTA adds the C slots in rank
+            // order, so all of them hold the same row totals and take the same branch below.
+            float4* slot = &xch[cpar];
+            cpar ^= 1;
+            if (tid == 0) *slot = make_float4(tot.hi, tot.lo, tmax, stop ? 1.0f : 0.0f);
+            cluster_sync();
+            FF sum{0.0f, 0.0f};
+            float mx = 0.0f;
+            bool any = false;
+            for (uint32_t k = 0; k < csize; ++k) {
+                const float4 v = ld_cluster_f4(smem_u32(slot), k);
+                if constexpr (EXACT) sum = ff_add(sum, FF{v.x, v.y});
+                else sum.hi = __fadd_rn(sum.hi, v.x);
+                mx = fmaxf(mx, v.z);
+                any = any || v.w != 0.0f;
+            }
+            tot = sum;
+            tmax = mx;
+            stop = any;
+        }
         if (stop) {
             if constexpr (RING) {
                 if (issuer) {
@@ -971,38 +1090,11 @@ rmsq_row_kernel(const Params p)
             if (issuer) refill(stage, stage_addr, true);
         }
         float rstd;
-        if constexpr (WARP_ROWS) {
-            // the warp's shuffles left the row's sum (and ONE_BAR's row max) in every lane
-            if constexpr (EXACT)
-                rstd = h_pow2 ? rstd_from_sum_pow2(ss, inv_h, p.eps) : rstd_from_sum(ss, Hf, p.eps);
-            else
-                rstd = __frsqrt_rn(__fadd_rn(__fmul_rn(ss.hi, inv_h), p.eps));
-        } else {
-            const float2 part = lane < nwarps ? red_ss[lane] : make_float2(0.0f, 0.0f);
-            if constexpr (EXACT) {
-                FF t{part.x, part.y};
-#pragma unroll
-                for (int o = 8; o > 0; o >>= 1)
-                    if (o < red_lanes) t = ff_add(t, shfl_xor_ff(t, o));
-                t.hi = __shfl_sync(0xFFFFFFFFu, t.hi, 0);
-                t.lo = __shfl_sync(0xFFFFFFFFu, t.lo, 0);
-                rstd = h_pow2 ? rstd_from_sum_pow2(t, inv_h, p.eps) : rstd_from_sum(t, Hf, p.eps);
-                if constexpr (ONE_BAR) {
-                    float m = lane < nwarps ? red_max[lane] : 0.0f;
-#pragma unroll
-                    for (int o = 8; o > 0; o >>= 1)
-                        if (o < red_lanes) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
-                    pmax = __shfl_sync(0xFFFFFFFFu, m, 0);
-                }
-            } else {
-                float t = part.x;
-#pragma unroll
-                for (int o = 8; o > 0; o >>= 1)
-                    if (o < red_lanes) t += __shfl_xor_sync(0xFFFFFFFFu, t, o);
-                t = __shfl_sync(0xFFFFFFFFu, t, 0);
-                rstd = __frsqrt_rn(__fadd_rn(__fmul_rn(t, inv_h), p.eps));
-            }
-        }
+        if constexpr (EXACT)
+            rstd = h_pow2 ? rstd_from_sum_pow2(tot, inv_h, p.eps) : rstd_from_sum(tot, Hf, p.eps);
+        else
+            rstd = __frsqrt_rn(__fadd_rn(__fmul_rn(tot.hi, inv_h), p.eps));
+        if constexpr (ONE_BAR) pmax = tmax;
         const float2 rstd2 = splat(rstd);
         // the residual sum s of vector k (zero past the row end)
         auto get_s = [&](int k) -> uint4 {
@@ -1079,25 +1171,35 @@ rmsq_row_kernel(const Params p)
                         if (o < red_lanes) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
                     amax = __shfl_sync(0xFFFFFFFFu, amax, 0);
                 }
+                if constexpr (CLUSTER) {
+                    float4* slot = &xch[2 + mpar];
+                    mpar ^= 1;
+                    if (tid == 0) *slot = make_float4(amax, 0.0f, 0.0f, 0.0f);
+                    cluster_sync();
+                    float mx = 0.0f;
+                    for (uint32_t k = 0; k < csize; ++k) mx = fmaxf(mx, ld_cluster_f4(smem_u32(slot), k).x);
+                    amax = mx;
+                }
             }
             float scale = __fdiv_rn(fminf(amax, p.scale_ub), 448.0f);
             if (p.scale_dtype == DT_BF16) {
                 uint16_t h;
                 asm("cvt.rn.bf16.f32 %0, %1;" : "=h"(h) : "f"(scale));
                 scale = __uint_as_float(static_cast<uint32_t>(h) << 16);
-                if (rt == 0) static_cast<uint16_t*>(p.scale_out)[row] = h;
+                if (rt == 0 && crank == 0) static_cast<uint16_t*>(p.scale_out)[row] = h;
             } else if (p.scale_dtype == DT_FP16) {
                 uint16_t h;
                 asm("cvt.rn.f16.f32 %0, %1;" : "=h"(h) : "f"(scale));
                 asm("cvt.f32.f16 %0, %1;" : "=f"(scale) : "h"(h));
-                if (rt == 0) static_cast<uint16_t*>(p.scale_out)[row] = h;
+                if (rt == 0 && crank == 0) static_cast<uint16_t*>(p.scale_out)[row] = h;
             } else {
-                if (rt == 0) static_cast<float*>(p.scale_out)[row] = scale;
+                if (rt == 0 && crank == 0) static_cast<float*>(p.scale_out)[row] = scale;
             }
             const bool zero_row = !(scale > 0.0f);
             const float2 inv2 = splat(zero_row ? 0.0f : __frcp_rn(scale));
             const float2 nd2 = splat(-scale);
-            unsigned char* outp = static_cast<unsigned char*>(p.out) + row * p.hidden;
+            unsigned char* outp = static_cast<unsigned char*>(p.out) + row * p.hidden +
+                                  static_cast<long long>(voff) * EPV;
 #pragma unroll
             for (int k = 0; k < VPT; ++k) {
                 const int v = rt + k * RT;
@@ -1142,7 +1244,8 @@ rmsq_row_kernel(const Params p)
             }
         } else if constexpr (NV_BLOCKED) {
             // ---- NVFP4, blocked: thread owns blocks b = rt + kb * RT (GROUP vectors each) -------
-            unsigned char* outp = static_cast<unsigned char*>(p.out) + row * (p.hidden / 2);
+            unsigned char* outp = static_cast<unsigned char*>(p.out) + row * (p.hidden / 2) +
+                                  static_cast<long long>(voff) * EPV / 2;
             unsigned char* sp_row = static_cast<unsigned char*>(p.scale_out) +
                 (p.swizzled ? (row >> 7) * (static_cast<long long>(p.k_tiles) * 512) +
                                   (row & 31) * 16 + ((row & 127) >> 5) * 4
@@ -1176,7 +1279,8 @@ rmsq_row_kernel(const Params p)
                 const float t = fminf(__fmul_rn(a, gs_over_6), 448.0f);
                 const uint32_t code = cvt_e4m3x2(t, 0.0f) & 0xFFu;
                 const float factor = nv_factor[code & 0x7Fu];
-                sp_row[p.swizzled ? (b >> 2) * 512 + (b & 3) : b] = static_cast<unsigned char>(code);
+                const int gb = sf_off + b;                                 // block in the row
+                sp_row[p.swizzled ? (gb >> 2) * 512 + (gb & 3) : gb] = static_cast<unsigned char>(code);
                 const bool zero_block = !(factor > 0.0f);
                 const float2 f2 = splat(zero_block ? 0.0f : __fmul_rn(factor, rstd));
                 uint32_t packed[GROUP];
@@ -1213,7 +1317,8 @@ rmsq_row_kernel(const Params p)
             // The block max of y is rstd * max |s w|, and the codes are E2M1(s w * rstd * factor)
             // with rstd folded into the block factor: for MXFP4 the factor is a power of two, so
             // the codes equal E2M1(RN(s w rstd) * 2^(127 - e)) whenever s w is exact.
-            unsigned char* outp = static_cast<unsigned char*>(p.out) + row * (p.hidden / 2);
+            unsigned char* outp = static_cast<unsigned char*>(p.out) + row * (p.hidden / 2) +
+                                  static_cast<long long>(voff) * EPV / 2;
             // scale byte of block sf sits at sp_row + col(sf): row-major sp + row * nsf + sf, or
             // the swizzled 128x4 tile position (row part here, scale part per block)
             unsigned char* sp_row = static_cast<unsigned char*>(p.scale_out) +
@@ -1243,7 +1348,7 @@ rmsq_row_kernel(const Params p)
                 if (v >= nv) continue;
                 if ((v & (GROUP - 1)) == 0)
                 {
-                    const int sf = v / GROUP;
+                    const int sf = sf_off + v / GROUP;
                     sp_row[p.swizzled ? (sf >> 2) * 512 + (sf & 3) : sf] = static_cast<unsigned char>(code);
                 }
                 const bool zero_block = !(factor > 0.0f);
@@ -1288,6 +1393,7 @@ rmsq_row_kernel(const Params p)
             }
         }
     }
+    if constexpr (CLUSTER) cluster_sync();   // no CTA leaves while others may read its slots
     if (aborted) return;
     if constexpr (MODE == MODE_AMAX) {
         // non-negative floats order like their bit patterns, so an unsigned max is a float max

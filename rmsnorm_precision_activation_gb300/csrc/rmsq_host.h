@@ -14,12 +14,13 @@ struct Plan {
     int dt;            // DT_*
     bool res;          // residual present
     int vpt;           // 16-byte vectors per thread per row: 1, 2, 4 or 8
-    int sched;         // SCHED_PIPE, SCHED_REG or SCHED_WARP
+    int sched;         // SCHED_PIPE, SCHED_REG, SCHED_WARP or SCHED_CLUSTER
     int threads;       // CTA size (multiple of 32); SCHED_WARP: 32 x rows in flight per CTA
     int stages;        // ring depth (SCHED_PIPE: per CTA, SCHED_WARP: per warp)
     int smem;          // dynamic shared memory bytes
     int ctas_per_sm;   // cap on resident CTAs per SM (0: occupancy limit)
     bool w16;          // 16-bit input and weight_offset 0: products from packed halves
+    int cluster = 1;   // SCHED_CLUSTER: CTAs per cluster (each takes 1/cluster of every row)
 };
 
 // Launch `fn` (a rmsq_row_kernel instantiation) with the plan: sets the dynamic shared memory
@@ -56,6 +57,9 @@ cudaError_t dispatch_amax(const Plan& plan, const Params& p, cudaStream_t stream
         switch (pl.sched) {                                                                       \
         case SCHED_PIPE: return NAME##_w16<DT, RES, VPT, SCHED_PIPE>(pl, p, st);                  \
         case SCHED_WARP: return NAME##_w16<DT, RES, VPT, SCHED_WARP>(pl, p, st);                  \
+        case SCHED_CLUSTER:                                                                       \
+            if constexpr (VPT >= 4) return NAME##_w16<DT, RES, VPT, SCHED_CLUSTER>(pl, p, st);    \
+            return cudaErrorInvalidConfiguration;                                                 \
         default: return NAME##_w16<DT, RES, VPT, SCHED_REG>(pl, p, st);                           \
         }                                                                                         \
     }                                                                                             \

@@ -50,7 +50,9 @@ def test_host_side_validation_without_gpu(lib):
     assert f(A, A, None, A, 4, 64, 0, 1e-6, 0.0, 1.0, A, A, 2, None) == 1
     assert f(A + 8, None, None, A, 4, 64, 0, 1e-6, 0.0, 1.0, A, A, 2, None) == 3
     assert f(A, None, None, A, 4, 60, 0, 1e-6, 0.0, 1.0, A, A, 2, None) == 2
-    assert f(A, None, None, A, 4, 65536, 0, 1e-6, 0.0, 1.0, A, A, 2, None) == 2
+    assert f(A, None, None, A, 4, 131072 + 256, 0, 1e-6, 0.0, 1.0, A, A, 2, None) == 2  # > max
+    assert f(A, None, None, A, 4, 65536 + 256, 2, 1e-6, 0.0, 1.0, A, A, 2, None) == 2   # fp32 > max
+    assert f(A, None, None, A, 4, 32768 + 8, 0, 1e-6, 0.0, 1.0, A, A, 2, None) == 2     # wide, not /256
     assert f(A, None, None, A, 4, 64, 3, 1e-6, 0.0, 1.0, A, A, 2, None) == 4
     assert f(A, None, None, A, 4, 64, 0, float("nan"), 0.0, 1.0, A, A, 2, None) == 6
     assert f(A, None, None, A, 4, 64, 0, 1e-6, 0.0, -1.0, A, A, 2, None) == 6
