@@ -10,7 +10,7 @@ Prints one JSON line:
             inputs resident in HBM, CUDA-event timed over exactly K steps
   e2e       the same metric through the public API with host buffers: pinned host -> device
             copies of the step's inputs and device -> host copies of its outputs inside the
-            timed region
+            timed region, overlapped with the kernels on separate copy streams
   roofline  the dominant kernel's achieved GB/s (its algorithmic bytes / its average launch time,
             events on its launching stream around its launches in every 10th timed step,
             from step 5 on)
@@ -341,31 +341,57 @@ def run_ours(args):
 
 def run_e2e(rq, step, device, K, world):
     """Same step through the public API, inputs from pinned host memory and outputs back to
-    pinned host memory inside the timed region."""
+    pinned host memory inside the timed region.
+
+    The three batches move through three streams, the way a caller overlaps transfers with
+    compute: one stream copies each batch's inputs in (pinned host -> device), the launch stream
+    runs the kernels, and one stream copies each batch's outputs back (device -> pinned host).
+    Events order each batch's copy-in, kernel and copy-out. They also stop a copy-in from
+    overwriting inputs that batch's previous kernel still reads, and a kernel from overwriting
+    outputs that are still being copied out."""
     host_in = {m: {k: v.cpu().pin_memory() for k, v in step.batches[m].items() if v is not None}
                for m in MODES}
     host_out = {m: tuple(torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in step.out[m])
                 for m in MODES}
     h2d = sum(t.numel() * t.element_size() for d in host_in.values() for t in d.values())
     d2h = sum(t.numel() * t.element_size() for o in host_out.values() for t in o)
-    stream = torch.cuda.current_stream(device)
+    compute = torch.cuda.current_stream(device)
+    s_in, s_out = torch.cuda.Stream(device), torch.cuda.Stream(device)
+    in_done = {m: torch.cuda.Event() for m in MODES}
+    ker_done = {m: torch.cuda.Event() for m in MODES}
+    out_done = {m: torch.cuda.Event() for m in MODES}
+    for m in MODES:
+        ker_done[m].record(compute)
+        out_done[m].record(compute)
 
     def one():
         for m in MODES:
-            for k, t in host_in[m].items():
-                step.batches[m][k].copy_(t, non_blocking=True)
-            step.launch(m)
-            for dst, src in zip(host_out[m], step.out[m]):
-                dst.copy_(src, non_blocking=True)
+            s_in.wait_event(ker_done[m])
+            with torch.cuda.stream(s_in):
+                for k, t in host_in[m].items():
+                    step.batches[m][k].copy_(t, non_blocking=True)
+            in_done[m].record(s_in)
+            compute.wait_event(in_done[m])
+            compute.wait_event(out_done[m])
+            step.launch(m, stream=compute)
+            ker_done[m].record(compute)
+            s_out.wait_event(ker_done[m])
+            with torch.cuda.stream(s_out):
+                for dst, src in zip(host_out[m], step.out[m]):
+                    dst.copy_(src, non_blocking=True)
+            out_done[m].record(s_out)
 
     one()
     torch.cuda.synchronize()
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier(world)
-    a.record(stream)
+    a.record(compute)
+    s_in.wait_event(a)
+    s_out.wait_event(a)
     for _ in range(K):
         one()
-    b.record(stream)
+    compute.wait_stream(s_out)
+    b.record(compute)
     torch.cuda.synchronize()
     value, ms = replica_throughput(step.step_bytes, K, world, a.elapsed_time(b))
     return {"value": round(value, 1), "unit": "GB/s",
