@@ -28,14 +28,38 @@ struct Plan {
 // than it takes to give each one a row; a row-per-warp CTA takes one row per warp).
 cudaError_t run_kernel(const void* fn, const Plan& plan, const Params& p, cudaStream_t stream);
 
-// Per-mode dispatch on (dtype, residual, vpt, schedule); defined in rmsq_<mode>.cu.
-cudaError_t dispatch_fp8(const Plan& plan, const Params& p, cudaStream_t stream);
-cudaError_t dispatch_nvfp4(const Plan& plan, const Params& p, cudaStream_t stream);
-cudaError_t dispatch_mxfp4(const Plan& plan, const Params& p, cudaStream_t stream);
-cudaError_t dispatch_amax(const Plan& plan, const Params& p, cudaStream_t stream);
+// Per-mode dispatch on (dtype, residual, vpt, schedule). Each quantisation mode's kernels are
+// split over two translation units, rmsq_<mode>.cu (no residual) and rmsq_<mode>_res.cu, so
+// the build compiles them in parallel (the amax pre-pass likewise).
+cudaError_t dispatch_fp8_plain(const Plan& plan, const Params& p, cudaStream_t stream);
+cudaError_t dispatch_fp8_res(const Plan& plan, const Params& p, cudaStream_t stream);
+cudaError_t dispatch_nvfp4_plain(const Plan& plan, const Params& p, cudaStream_t stream);
+cudaError_t dispatch_nvfp4_res(const Plan& plan, const Params& p, cudaStream_t stream);
+cudaError_t dispatch_mxfp4_plain(const Plan& plan, const Params& p, cudaStream_t stream);
+cudaError_t dispatch_mxfp4_res(const Plan& plan, const Params& p, cudaStream_t stream);
+cudaError_t dispatch_amax_plain(const Plan& plan, const Params& p, cudaStream_t stream);
+cudaError_t dispatch_amax_res(const Plan& plan, const Params& p, cudaStream_t stream);
 
-// Instantiates the dispatch switch for one mode inside a .cu file.
-#define RMSQ_DEFINE_DISPATCH(NAME, MODE)                                                         \
+inline cudaError_t dispatch_fp8(const Plan& pl, const Params& p, cudaStream_t st)
+{
+    return pl.res ? dispatch_fp8_res(pl, p, st) : dispatch_fp8_plain(pl, p, st);
+}
+inline cudaError_t dispatch_nvfp4(const Plan& pl, const Params& p, cudaStream_t st)
+{
+    return pl.res ? dispatch_nvfp4_res(pl, p, st) : dispatch_nvfp4_plain(pl, p, st);
+}
+inline cudaError_t dispatch_mxfp4(const Plan& pl, const Params& p, cudaStream_t st)
+{
+    return pl.res ? dispatch_mxfp4_res(pl, p, st) : dispatch_mxfp4_plain(pl, p, st);
+}
+inline cudaError_t dispatch_amax(const Plan& pl, const Params& p, cudaStream_t st)
+{
+    return pl.res ? dispatch_amax_res(pl, p, st) : dispatch_amax_plain(pl, p, st);
+}
+
+// Instantiates the dispatch switch of one mode, for one residual case (RESV), inside a .cu file.
+#define RMSQ_DEFINE_DISPATCH_FOR(NAME, MODE, RESV) RMSQ_DEFINE_DISPATCH_IMPL(NAME, MODE, !(RESV), RESV)
+#define RMSQ_DEFINE_DISPATCH_IMPL(NAME, MODE, PLAIN_OK, RES_OK)                                  \
     template <int DT, bool RES, int VPT, int SCHED, bool W16>                                     \
     static cudaError_t NAME##_go(const Plan& pl, const Params& p, cudaStream_t st)                \
     {                                                                                             \
@@ -76,7 +100,12 @@ cudaError_t dispatch_amax(const Plan& plan, const Params& p, cudaStream_t stream
     template <int DT>                                                                             \
     static cudaError_t NAME##_res(const Plan& pl, const Params& p, cudaStream_t st)               \
     {                                                                                             \
-        return pl.res ? NAME##_vpt<DT, true>(pl, p, st) : NAME##_vpt<DT, false>(pl, p, st);      \
+        if (pl.res) {                                                                             \
+            if constexpr (RES_OK) return NAME##_vpt<DT, true>(pl, p, st);                         \
+        } else {                                                                                  \
+            if constexpr (PLAIN_OK) return NAME##_vpt<DT, false>(pl, p, st);                      \
+        }                                                                                         \
+        return cudaErrorInvalidValue;                                                             \
     }                                                                                             \
     cudaError_t NAME(const Plan& pl, const Params& p, cudaStream_t st)                            \
     {                                                                                             \
