@@ -1,16 +1,18 @@
 // rmsq_device.cuh -- device code of the fused residual-add + RMSNorm + FP8 / NVFP4 / MXFP4 kernels
 // for sm_103a (GB300).
 //
-// One kernel template covers every mode, input type and schedule. A CTA owns whole rows: its T
-// threads split a row into 16-byte vectors (vector v of the row goes to thread v % T, so a warp
-// touches 512 contiguous bytes per step), add the residual, reduce the sum of squares over the
-// CTA, form y = s * rstd * (gamma + offset) and quantise. The row is read from HBM exactly once.
+// One kernel template covers every mode, input type and schedule. A row processor (a CTA, a warp
+// or a cluster) owns whole rows: its threads split a row into 16-byte vectors (vector v goes to
+// thread v % T, so a warp touches 512 contiguous bytes per step), add the residual, reduce the
+// sum of squares, form y = s * rstd * (gamma + offset) and quantise. The row is read from HBM
+// exactly once.
 //
-// Three schedules fetch the row:
+// Four schedules fetch the row:
 //   SCHED_PIPE  persistent CTAs with a ring of `stages` shared-memory row buffers filled by the
 //               TMA bulk-copy engine (cp.async.bulk + mbarrier transaction counts). Thread 0
-//               refills a buffer with the row `stages` iterations ahead as soon as the CTA has
-//               read it, so several rows per SM stay in flight while the CTA computes.
+//               refills a buffer with the CTA's next row as soon as the CTA has read it, so
+//               several rows per SM stay in flight while the CTA computes. Rows are dealt out
+//               round-robin, the last quarter one at a time from a per-launch counter.
 //   SCHED_REG   persistent CTAs that load their row straight into registers with 128-bit
 //               streaming loads; latency is hidden by the other CTAs on the SM.
 //   SCHED_WARP  row per warp, for short rows: every warp of a CTA owns whole rows with its own
@@ -1375,7 +1377,7 @@ rmsq_row_kernel(const Params p)
             }
         }
         if constexpr (SMEM_S) {
-            // Every thread is done with this slot: refill it with the row S iterations ahead.
+            // Every thread is done with this slot: refill it with the ring's next row.
             // (Each lane wrote s into the slot; in the row-per-warp schedule every lane orders
             // its writes before the refill's async-proxy writes.)
             if constexpr (WARP_ROWS) {
