@@ -118,3 +118,19 @@ def check_mxfp4(w: W.Workload, d: dict, idx=None, swizzled=False):
                              host_bits(g), dtype=ODT[x.dtype], eps=w.eps,
                              weight_offset=w.weight_offset, want_y=True, want_pre=True)
     return P.compare_mxfp4(gq, gbs, gro, ora).check(), (q, bs, ro)
+
+
+GUARD = 4096       # canary bytes after every guarded output
+GUARD_FILL = 0x5A
+
+
+def guarded(n, dtype):
+    """An output of n elements of dtype followed by GUARD canary bytes; returns (view, raw). A
+    kernel that writes past the output changes raw[-GUARD:]."""
+    itemsize = torch.empty(0, dtype=dtype).element_size()
+    raw = torch.full((n * itemsize + GUARD,), GUARD_FILL, dtype=torch.uint8, device="cuda")
+    return raw[: n * itemsize].view(dtype), raw
+
+
+def guards_intact(raws) -> bool:
+    return all(bool(torch.all(raw[-GUARD:] == GUARD_FILL)) for raw in raws)

@@ -13,8 +13,8 @@ import pytest
 import torch
 
 import workloads as W
-from gpu_common import (check_fp8, check_mxfp4, check_nvfp4, inputs, oracle_global_scale, rq,
-                        schedule)
+from gpu_common import (check_fp8, check_mxfp4, check_nvfp4, guarded, guards_intact, inputs,
+                        oracle_global_scale, rq, schedule)
 
 pytestmark = pytest.mark.gpu
 
@@ -112,13 +112,6 @@ def test_wide_rows_guard_bytes(mode):
     rows, H = 5, 65536 + 256
     w = W.Workload("custom", mode, rows, H, "bf16", True)
     d = W.generate(w, seed=23, device="cuda")
-    guard = 4096
-
-    def guarded(n, dtype):
-        itemsize = torch.empty(0, dtype=dtype).element_size()
-        raw = torch.full((n * itemsize + guard,), 0x5A, dtype=torch.uint8, device="cuda")
-        return raw[: n * itemsize].view(dtype), raw
-
     ro, ro_raw = guarded(rows * H, torch.bfloat16)
     ro = ro.view(rows, H)
     if mode == "fp8":
@@ -134,7 +127,6 @@ def test_wide_rows_guard_bytes(mode):
                                  output=q.view(rows, H // 2), block_scale=b.view(rows, H // 32))
         raws = (ro_raw, q_raw, b_raw)
     torch.cuda.synchronize()
-    for raw in raws:
-        assert torch.all(raw[-guard:] == 0x5A)
+    assert guards_intact(raws)
     assert torch.equal(ro, (d["input"].float() + d["residual"].float()).to(torch.bfloat16))
     assert rq().rmsq_device_status() == 0

@@ -8,19 +8,9 @@ import torch
 
 import oracle
 import workloads as W
-from gpu_common import check_fp8, check_mxfp4, check_nvfp4, host_bits, rq
+from gpu_common import check_fp8, check_mxfp4, check_nvfp4, guarded, guards_intact, host_bits, rq
 
 pytestmark = pytest.mark.gpu
-
-GUARD = 4096
-
-
-def _guarded(n, dtype, fill=0x5A):
-    """A uint8 buffer with GUARD canary bytes after n elements; returns (view, raw)."""
-    itemsize = torch.empty(0, dtype=dtype).element_size()
-    raw = torch.full((n * itemsize + GUARD,), fill, dtype=torch.uint8, device="cuda")
-    return raw[: n * itemsize].view(dtype), raw
-
 
 def test_empty_call_launches_nothing():
     x = torch.empty(0, 4096, dtype=torch.bfloat16, device="cuda")
@@ -38,20 +28,20 @@ def test_guard_bytes_untouched(mode, sched):
     rows, H = 97, 2080
     w = W.Workload("custom", mode, rows, H, "bf16", True)
     d = W.generate(w, seed=21, device="cuda")
-    ro, ro_raw = _guarded(rows * H, torch.bfloat16)
+    ro, ro_raw = guarded(rows * H, torch.bfloat16)
     ro = ro.view(rows, H)
     prev = rq().rmsq_set_schedule(sched)
     try:
         if mode == "fp8":
-            q, q_raw = _guarded(rows * H, torch.uint8)
-            s, s_raw = _guarded(rows, torch.float32)
+            q, q_raw = guarded(rows * H, torch.uint8)
+            s, s_raw = guarded(rows, torch.float32)
             rq().rmsnorm_quant_fp8(d["input"], d["gamma"], residual=d["residual"], residual_output=ro,
                                    output=q.view(rows, H).view(torch.float8_e4m3fn), scale_output=s)
             raws = (ro_raw, q_raw, s_raw)
         else:
             blk = 16 if mode == "nvfp4" else 32
-            q, q_raw = _guarded(rows * H // 2, torch.uint8)
-            b, b_raw = _guarded(rows * H // blk, torch.uint8)
+            q, q_raw = guarded(rows * H // 2, torch.uint8)
+            b, b_raw = guarded(rows * H // blk, torch.uint8)
             fn = rq().rmsnorm_quant_nvfp4 if mode == "nvfp4" else rq().rmsnorm_quant_mxfp4
             bs = b.view(rows, H // blk)
             fn(d["input"], d["gamma"], residual=d["residual"], residual_output=ro,
@@ -60,8 +50,7 @@ def test_guard_bytes_untouched(mode, sched):
     finally:
         rq().rmsq_set_schedule(prev)
     torch.cuda.synchronize()
-    for raw in raws:
-        assert torch.all(raw[-GUARD:] == 0x5A)
+    assert guards_intact(raws)
     assert torch.equal(ro, (d["input"].float() + d["residual"].float()).to(torch.bfloat16))
 
 

@@ -9,8 +9,8 @@ import pytest
 import torch
 
 import workloads as W
-from gpu_common import (check_fp8, check_mxfp4, check_nvfp4, inputs, oracle_global_scale, rq,
-                        sample_rows, schedule)
+from gpu_common import (check_fp8, check_mxfp4, check_nvfp4, guarded, guards_intact, inputs,
+                        oracle_global_scale, rq, sample_rows, schedule)
 
 pytestmark = pytest.mark.gpu
 
@@ -141,13 +141,6 @@ def test_warp_rows_guard_bytes(mode):
     rows, H = 97, 2016
     w = W.Workload("custom", mode, rows, H, "bf16", True)
     d = W.generate(w, seed=22, device="cuda")
-    guard = 4096
-
-    def guarded(n, dtype):
-        itemsize = torch.empty(0, dtype=dtype).element_size()
-        raw = torch.full((n * itemsize + guard,), 0x5A, dtype=torch.uint8, device="cuda")
-        return raw[: n * itemsize].view(dtype), raw
-
     ro, ro_raw = guarded(rows * H, torch.bfloat16)
     ro = ro.view(rows, H)
     with schedule(WARP):
@@ -172,6 +165,5 @@ def test_warp_rows_guard_bytes(mode):
                                          block_scale=bs)
             raws = (ro_raw, q_raw, b_raw)
     torch.cuda.synchronize()
-    for raw in raws:
-        assert torch.all(raw[-guard:] == 0x5A)
+    assert guards_intact(raws)
     assert torch.equal(ro, (d["input"].float() + d["residual"].float()).to(torch.bfloat16))
