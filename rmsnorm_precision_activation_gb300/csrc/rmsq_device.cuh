@@ -1202,11 +1202,8 @@ rmsq_row_kernel(const Params p)
             const float2 nd2 = splat(-scale);
             unsigned char* outp = static_cast<unsigned char*>(p.out) + row * p.hidden +
                                   static_cast<long long>(voff) * EPV;
-#pragma unroll
-            for (int k = 0; k < VPT; ++k) {
-                const int v = rt + k * RT;
-                if (v >= nv) continue;
-                float2 yk[NP];
+            // y of vector k of this thread
+            auto y_of = [&](int k, float2 (&yk)[NP]) {
                 if constexpr (KEEP_Y) {
 #pragma unroll
                     for (int j = 0; j < NP; ++j) yk[j] = y[k][j];
@@ -1221,20 +1218,8 @@ rmsq_row_kernel(const Params p)
 #pragma unroll
                     for (int j = 0; j < NP; ++j) yk[j] = norm_mul2(f[j], w[j], rstd2);
                 }
-                float2 q[NP];
-                uint32_t key = 0xFFFFFFFFu;
-#pragma unroll
-                for (int j = 0; j < NP; ++j) {
-                    q[j] = div_rn2(yk[j], nd2, inv2);
-                    key = min(key, min(tie_key(q[j].x), tie_key(q[j].y)));
-                }
-                if (key == 0u) {           // rare: a quotient sits on an E4M3 boundary
-#pragma unroll
-                    for (int j = 0; j < NP; ++j) {
-                        q[j].x = untie(q[j].x, yk[j].x, nd2.x);
-                        q[j].y = untie(q[j].y, yk[j].y, nd2.y);
-                    }
-                }
+            };
+            auto store_codes = [&](int v, const float2 (&q)[NP]) {
                 uint32_t c[NP];
 #pragma unroll
                 for (int j = 0; j < NP; ++j) c[j] = zero_row ? 0u : cvt_e4m3x2(q[j].x, q[j].y);
@@ -1242,6 +1227,68 @@ rmsq_row_kernel(const Params p)
                     st_v2(outp + v * 8, c[0] | (c[1] << 16), c[2] | (c[3] << 16));
                 } else {
                     st_u32(outp + v * 4, c[0] | (c[1] << 16));
+                }
+            };
+            if constexpr (W16) {
+                // With 16-bit products, quotients land exactly on an E4M3 boundary often enough
+                // (448 * P_i / P_max, a ratio of short numbers) that the fix-up stays per vector,
+                // on the 8 values at hand.
+#pragma unroll
+                for (int k = 0; k < VPT; ++k) {
+                    const int v = rt + k * RT;
+                    if (v >= nv) continue;
+                    float2 yk[NP], q[NP];
+                    y_of(k, yk);
+                    uint32_t key = 0xFFFFFFFFu;
+#pragma unroll
+                    for (int j = 0; j < NP; ++j) {
+                        q[j] = div_rn2(yk[j], nd2, inv2);
+                        key = min(key, min(tie_key(q[j].x), tie_key(q[j].y)));
+                    }
+                    if (key == 0u) {
+#pragma unroll
+                        for (int j = 0; j < NP; ++j) {
+                            q[j].x = untie(q[j].x, yk[j].x, nd2.x);
+                            q[j].y = untie(q[j].y, yk[j].y, nd2.y);
+                        }
+                    }
+                    store_codes(v, q);
+                }
+            } else {
+                // Otherwise such quotients are rare (about 2^-19 of them), so the common path has
+                // no branch per vector and the vectors' work interleaves: the correctly rounded
+                // quotients go straight to E4M3 and the tie keys are folded over the row. A
+                // thread that met a boundary redoes its vectors with the fix-up and stores them
+                // again.
+                uint32_t key = 0xFFFFFFFFu;
+#pragma unroll
+                for (int k = 0; k < VPT; ++k) {
+                    const int v = rt + k * RT;
+                    if (v >= nv) continue;
+                    float2 yk[NP], q[NP];
+                    y_of(k, yk);
+#pragma unroll
+                    for (int j = 0; j < NP; ++j) {
+                        q[j] = div_rn2(yk[j], nd2, inv2);
+                        key = min(key, min(tie_key(q[j].x), tie_key(q[j].y)));
+                    }
+                    store_codes(v, q);
+                }
+                if (key == 0u) {
+#pragma unroll
+                    for (int k = 0; k < VPT; ++k) {
+                        const int v = rt + k * RT;
+                        if (v >= nv) continue;
+                        float2 yk[NP], q[NP];
+                        y_of(k, yk);
+#pragma unroll
+                        for (int j = 0; j < NP; ++j) {
+                            q[j] = div_rn2(yk[j], nd2, inv2);
+                            q[j].x = untie(q[j].x, yk[j].x, nd2.x);
+                            q[j].y = untie(q[j].y, yk[j].y, nd2.y);
+                        }
+                        store_codes(v, q);
+                    }
                 }
             }
         } else if constexpr (NV_BLOCKED) {
