@@ -10,11 +10,13 @@ Prints one JSON line:
             inputs resident in HBM, CUDA-event timed over exactly K steps
   e2e       the same metric through the public API with host buffers: pinned host -> device
             copies of the step's inputs and device -> host copies of its outputs inside the
-            timed region, overlapped with the kernels on separate copy streams
+            timed region, overlapped with the kernels on separate copy streams; beside it, the
+            same copies timed alone (the floor the host link sets)
   roofline  the dominant kernel's achieved GB/s (its algorithmic bytes / its average launch time,
             events on its launching stream around its launches in every 10th timed step,
             from step 5 on)
-            against the measured HBM copy bandwidth
+            against the measured HBM copy bandwidth; beside it, what a plain device copy of
+            the same bytes reaches
   cpu_baseline  the oracle on a bounded sample of the same workload, on this host's cores
 
 --impl reference times the oracle itself as the reference arm. --report runs every workload
@@ -221,6 +223,29 @@ def replica_throughput(step_bytes, steps, world, local_ms):
     return step_bytes * steps * world / (ms * 1e-3) / 1e9, ms
 
 
+def same_bytes_copy_gbs(nbytes, device, reps=10):
+    """GB/s of a plain device-to-device copy that moves `nbytes` (half read, half written), the
+    size of one launch. L2 is filled with clean lines by a 256 MiB read before each copy, so the
+    copy reads from DRAM as the kernels do. Median of `reps` event-timed copies after 3
+    warm-ups. Reported beside the roofline: a launch of this size cannot run at the bandwidth of
+    the multi-GB copy the peak comes from, and this says what a copy reaches at the same size."""
+    n = nbytes // 2 // 16 * 16
+    src = torch.full((n,), 3, dtype=torch.uint8, device=device)
+    dst = torch.empty_like(src)
+    flush = torch.ones(64 << 20, dtype=torch.float32, device=device)
+    times = []
+    for i in range(reps + 3):
+        flush.amax()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        dst.copy_(src)
+        b.record()
+        torch.cuda.synchronize()
+        if i >= 3:
+            times.append(a.elapsed_time(b))
+    return 2 * n / statistics.median(times) / 1e6
+
+
 def barrier(world):
     if world > 1:
         import torch.distributed as dist
@@ -290,6 +315,7 @@ def run_ours(args):
     dom = max(per_mode_ms, key=per_mode_ms.get)
     dom_gbs = step.bytes[dom] / (per_mode_ms[dom] * 1e-3) / 1e9
     peak, peak_src = measured_peak()
+    copy_gbs = same_bytes_copy_gbs(step.bytes[dom], device)
     kname = {"fp8": "rmsnorm_quant_fp8", "nvfp4": "rmsnorm_quant_nvfp4",
              "mxfp4": "rmsnorm_quant_mxfp4"}[dom]
     line = {
@@ -325,7 +351,8 @@ def run_ours(args):
                      "traffic": recorded_traffic(kname),
                      "timing": "CUDA events around each launch of timed steps %s"
                                % ",".join(str(i) for i in probed),
-                     "algorithmic_bytes_per_launch": step.bytes[dom]},
+                     "algorithmic_bytes_per_launch": step.bytes[dom],
+                     "copy_same_bytes_gbs": round(copy_gbs, 1)},
         "e2e": e2e,
         "gpu_launches": int(launches),
         "clocks": clocks.summary(),
@@ -394,9 +421,36 @@ def run_e2e(rq, step, device, K, world):
     b.record(compute)
     torch.cuda.synchronize()
     value, ms = replica_throughput(step.step_bytes, K, world, a.elapsed_time(b))
+
+    # The same copies with no kernels and no ordering between the two directions: the floor the
+    # host link sets under the end-to-end step. Timed after the step, outside its timed region.
+    def copies_only():
+        for m in MODES:
+            with torch.cuda.stream(s_in):
+                for k, t in host_in[m].items():
+                    step.batches[m][k].copy_(t, non_blocking=True)
+            with torch.cuda.stream(s_out):
+                for dst, src in zip(host_out[m], step.out[m]):
+                    dst.copy_(src, non_blocking=True)
+
+    copies_only()
+    torch.cuda.synchronize()
+    c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    c0.record(compute)
+    s_in.wait_event(c0)
+    s_out.wait_event(c0)
+    for _ in range(K):
+        copies_only()
+    compute.wait_stream(s_in)
+    compute.wait_stream(s_out)
+    c1.record(compute)
+    torch.cuda.synchronize()
+    copy_ms = c0.elapsed_time(c1) / K
     return {"value": round(value, 1), "unit": "GB/s",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-            "ms_per_step": round(ms / K, 4), "steps": K}
+            "ms_per_step": round(ms / K, 4), "steps": K,
+            "copies_only_ms_per_step": round(copy_ms, 4),
+            "copies_only_GBs": round((h2d + d2h) / copy_ms / 1e6, 1)}
 
 
 # ------------------------------------------------------------------------------------------
