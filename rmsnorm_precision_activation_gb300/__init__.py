@@ -23,7 +23,9 @@ LIB_PATH = os.path.join(_HERE, "librmsq.so")
 RMSQ_BF16, RMSQ_FP16, RMSQ_F32 = 0, 1, 2
 SCALE_ROW_MAJOR, SCALE_SWIZZLED_128x4 = 0, 1
 SCHED_AUTO, SCHED_PIPE, SCHED_REG, SCHED_WARP, SCHED_CLUSTER = 0, 1, 2, 3, 4
-MAX_HIDDEN = 32768
+# Widest row accepted, in elements (fp32 input: half). Rows wider than ONE_CTA_HIDDEN (fp32:
+# half) run on a thread-block cluster and must be a multiple of 256 elements.
+MAX_HIDDEN, ONE_CTA_HIDDEN = 131072, 32768
 
 STATUS = {0: "RMSQ_OK", 1: "RMSQ_ERR_NULL", 2: "RMSQ_ERR_SHAPE", 3: "RMSQ_ERR_ALIGN",
           4: "RMSQ_ERR_DTYPE", 5: "RMSQ_ERR_LAUNCH", 6: "RMSQ_ERR_VALUE", 7: "RMSQ_ERR_DEVICE",

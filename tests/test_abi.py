@@ -37,6 +37,18 @@ def test_library_exports_every_declared_symbol(lib):
         assert n in rq.SIGNATURES, n
 
 
+def test_python_constants_match_the_header():
+    import rmsnorm_precision_activation_gb300 as rq
+    src = open(os.path.join(ROOT, "include", "rmsq.h")).read()
+    define = lambda n: int(re.search(r"#define %s (\d+)" % n, src).group(1))
+    assert rq.MAX_HIDDEN == define("RMSQ_MAX_HIDDEN")
+    assert rq.ONE_CTA_HIDDEN == define("RMSQ_ONE_CTA_HIDDEN")
+    for code, name in rq.STATUS.items():
+        assert re.search(r"\b%s = %d\b" % (name, code), src), name
+    for name in ("RMSQ_BF16", "RMSQ_FP16", "RMSQ_F32"):
+        assert re.search(r"\b%s = %d\b" % (name, getattr(rq, name)), src), name
+
+
 def test_status_strings(lib):
     for code, name in [(0, "RMSQ_OK"), (2, "RMSQ_ERR_SHAPE"), (8, "RMSQ_ERR_TIMEOUT")]:
         assert lib.rmsq_status_string(code).decode().startswith(name)
