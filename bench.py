@@ -672,6 +672,130 @@ def run_report(args):
         print(json.dumps(line), flush=True)
 
 
+def next_row_cases():
+    """The widened rows, each as (row, case, workload, options). Options: `swizzled` (128x4
+    scale layout), `prepass` (time the NVFP4 global-scale pre-pass instead of the quantiser),
+    `dtype` (input dtype other than the workload's), `scale_dtype` (FP8 scale output type)."""
+    nv = W.config("nvfp4")
+    mx = W.config("mxfp4_residual", rows=65536, hidden=8192)
+    f8 = W.config("fp8_residual")
+
+    def wide(mode, rows, hidden):
+        return W.Workload("wide_rows", mode, rows, hidden, "bf16", True, scale_ub=1200.0)
+
+    return [
+        ("NEXT-1", "swizzled_scales", nv, {"swizzled": True}),
+        ("NEXT-1", "swizzled_scales", mx, {"swizzled": True}),
+        ("NEXT-2", "global_scale_prepass", nv, {"prepass": True}),
+        ("NEXT-2", "global_scale_prepass", W.Workload("nvfp4_residual", "nvfp4", 8192, 4096,
+                                                      "bf16", True), {"prepass": True}),
+        ("NEXT-3", "fp32_input", f8, {"dtype": torch.float32}),
+        ("NEXT-3", "fp32_input", W.config("mxfp4_residual", rows=4096, hidden=16384),
+         {"dtype": torch.float32}),
+        ("NEXT-3", "fp16_input", nv, {"dtype": torch.float16}),
+        ("NEXT-3", "fp16_input", mx, {"dtype": torch.float16}),
+        ("NEXT-3", "bf16_scale_output", f8, {"scale_dtype": torch.bfloat16}),
+        ("NEXT-4", "cluster_rows", wide("fp8", 4096, 65536), {}),
+        ("NEXT-4", "cluster_rows", wide("nvfp4", 4096, 65536), {}),
+        ("NEXT-4", "cluster_rows", wide("mxfp4", 4096, 65536), {}),
+        ("NEXT-4", "cluster_rows", wide("fp8", 2048, 131072), {}),
+        ("NEXT-4", "cluster_rows", wide("nvfp4", 2048, 131072), {}),
+        ("NEXT-4", "cluster_rows", wide("mxfp4", 2048, 131072), {}),
+    ]
+
+
+def variant_bytes(w, opts):
+    """Algorithmic bytes of one launch of workload w under `opts` (see next_row_cases): inputs
+    read and outputs written once, gamma once per launch. The swizzled layout writes the same
+    scale bytes when rows are a multiple of 128 and the scale columns a multiple of 4."""
+    e = torch.tensor([], dtype=opts.get("dtype", w.torch_dtype)).element_size()
+    n = w.rows * w.hidden
+    read = n * e * (2 if w.residual else 1) + w.hidden * e
+    if opts.get("prepass"):
+        return read + 4                              # max |y| as one fp32 value
+    write = n * e if w.residual else 0
+    if w.mode == "fp8":
+        sd = opts.get("scale_dtype", torch.float32)
+        write += n + w.rows * torch.tensor([], dtype=sd).element_size()
+    elif w.mode == "nvfp4":
+        read += 4
+        write += n // 2 + n // 16
+    else:
+        write += n // 2 + n // 32
+    return read + write
+
+
+def _time_launch(fn, flush, reps):
+    fn()
+    for _ in range(3):
+        fn()
+    times = []
+    for _ in range(reps):
+        flush.fill_(1)                               # evict L2 between repetitions
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        fn()
+        b.record()
+        b.synchronize()
+        times.append(a.elapsed_time(b))
+    return statistics.median(times) * 1e3
+
+
+def run_report_next(args):
+    """One JSON line per widened-row case: its event-timed duration and algorithmic GB/s, and
+    beside it the same workload with the default options (`base_us`), where there is one."""
+    from rmsnorm_precision_activation_gb300 import build as B
+    B.build()
+    import rmsnorm_precision_activation_gb300 as rq
+    torch.cuda.set_device(0)
+    peak, _ = measured_peak()
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+
+    def launcher(w, d, opts):
+        x, r, g = d["input"], d["residual"], d["gamma"]
+        sw = opts.get("swizzled", False)
+        if opts.get("prepass"):
+            return lambda: rq.rmsnorm_nvfp4_global_scale(x, g, residual=r, epsilon=w.eps)
+        if w.mode == "fp8":
+            sd = opts.get("scale_dtype", torch.float32)
+            return lambda: rq.rmsnorm_quant_fp8(x, g, residual=r, epsilon=w.eps,
+                                                weight_offset=w.weight_offset,
+                                                scale_ub=w.scale_ub, scale_dtype=sd)
+        if w.mode == "nvfp4":
+            gs = torch.full((1,), 2.0, dtype=torch.float32, device="cuda")
+            return lambda: rq.rmsnorm_quant_nvfp4(x, g, global_scale=gs, residual=r,
+                                                  epsilon=w.eps, swizzled=sw)
+        return lambda: rq.rmsnorm_quant_mxfp4(x, g, residual=r, epsilon=w.eps, swizzled=sw)
+
+    for row, case, w, opts in next_row_cases():
+        d = W.generate(w, seed=0, device="cuda")
+        if "dtype" in opts:
+            d = {k: (None if v is None else v.to(opts["dtype"])) for k, v in d.items()}
+        us = _time_launch(launcher(w, d, opts), flush, args.report_reps)
+        nb = variant_bytes(w, opts)
+        io = {torch.float32: "fp32", torch.float16: "fp16", torch.bfloat16: "bf16"}[d["input"].dtype]
+        line = {"row": row, "case": case, "workload": w.name, "shape": [w.rows, w.hidden],
+                "mode": w.mode, "io_dtype": io, "residual": w.residual,
+                "options": {k: (str(v).replace("torch.", "") if isinstance(v, torch.dtype) else v)
+                            for k, v in opts.items()},
+                "us": round(us, 2), "algorithmic_bytes": nb, "gbs": round(nb / (us * 1e-6) / 1e9, 1),
+                "frac_of_measured": round(nb / (us * 1e-6) / 1e9 / peak, 4)}
+        if case in ("fp32_input", "fp16_input"):
+            db = W.generate(w, seed=0, device="cuda")
+            line["base_us"] = round(_time_launch(launcher(w, db, {}), flush, args.report_reps), 2)
+            line["base"] = "%s input" % w.dtype
+            del db
+        elif case != "cluster_rows":
+            line["base_us"] = round(_time_launch(launcher(w, d, {}), flush, args.report_reps), 2)
+            line["base"] = {"swizzled_scales": "row-major scales",
+                            "global_scale_prepass": "the NVFP4 quantiser on the same input",
+                            "bf16_scale_output": "fp32 scale output"}[case]
+        print(json.dumps(line), flush=True)
+        del d
+        torch.cuda.empty_cache()
+    assert rq.rmsq_device_status() == 0
+
+
 # ------------------------------------------------------------------------------------------
 # ncu-backed per-workload table
 # ------------------------------------------------------------------------------------------
@@ -738,6 +862,9 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--report", action="store_true", help="per-workload GB/s lines")
     ap.add_argument("--report-reps", type=int, default=20)
+    ap.add_argument("--report-next", action="store_true",
+                    help="time the widened rows (swizzled scales, global-scale pre-pass, other "
+                         "dtypes, cluster rows), one JSON line each")
     ap.add_argument("--only", default="", help="--report: comma-separated workload names "
                     "(or name:rows:hidden for one MXFP4 sweep point)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -756,6 +883,8 @@ def main():
         ncu_table(args)
     elif args.impl == "reference":
         run_reference(args)
+    elif args.report_next:
+        run_report_next(args)
     elif args.report:
         run_report(args)
     else:
