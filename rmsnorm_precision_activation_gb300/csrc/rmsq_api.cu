@@ -293,12 +293,17 @@ static bool make_plan(int mode, int dt, bool res, bool w16, int hidden, const De
             const long long cstage = static_cast<long long>(nvc) * 16 * (res ? 2 : 1);
             int cv = 4;
             while (cv < 8 && nvc > 256 * cv) cv *= 2;
+            // ring slots, reduction area, per slot an mbarrier and a row number, exchange slots
+            int stages = g_tune_stages.load();
+            if (stages < 2) stages = 2;
+            auto cbytes = [&](int st) { return st * cstage + red_bytes + st * 16 + kClusterXchBytes; };
+            while (stages > 2 && cbytes(stages) > di.smem_optin) --stages;
             pl.sched = SCHED_CLUSTER;
             pl.cluster = best;
             pl.vpt = cv;
             pl.threads = ((nvc + cv - 1) / cv + 31) / 32 * 32;
-            pl.stages = 2;
-            pl.smem = static_cast<int>(2 * cstage + red_bytes + 2 * 16 + kClusterXchBytes);
+            pl.stages = stages;
+            pl.smem = static_cast<int>(cbytes(stages));
             pl.ctas_per_sm = 0;
             return true;
         }

@@ -130,3 +130,35 @@ def test_wide_rows_guard_bytes(mode):
     assert guards_intact(raws)
     assert torch.equal(ro, (d["input"].float() + d["residual"].float()).to(torch.bfloat16))
     assert rq().rmsq_device_status() == 0
+
+
+def _launch(mode, d):
+    x, r, g = d["input"], d["residual"], d["gamma"]
+    if mode == "fp8":
+        return rq().rmsnorm_quant_fp8(x, g, residual=r, scale_ub=1200.0)
+    if mode == "nvfp4":
+        gs = torch.full((1,), 2.0, dtype=torch.float32, device=x.device)
+        return rq().rmsnorm_quant_nvfp4(x, g, global_scale=gs, residual=r)
+    return rq().rmsnorm_quant_mxfp4(x, g, residual=r)
+
+
+def _bits(outs):
+    return [o.view(torch.uint8) if o.dtype == torch.float8_e4m3fn else o for o in outs]
+
+
+@pytest.mark.parametrize("mode", ["fp8", "nvfp4", "mxfp4"])
+def test_cluster_ring_depth_leaves_every_bit(mode):
+    # deeper rings only change when slices arrive, never the arithmetic
+    w = W.Workload("custom", mode, 200, 65536, "bf16", True, scale_ub=1200.0)
+    d = inputs(w, seed=61)
+    ref = _bits(_launch(mode, d))
+    for stages in (3, 4):
+        rq().rmsq_set_tuning(stages, 0, 0)
+        try:
+            got = _bits(_launch(mode, d))
+        finally:
+            rq().rmsq_set_tuning(0, 0, 0)
+        torch.cuda.synchronize()
+        assert all(torch.equal(a, b) for a, b in zip(got, ref)), stages
+    _check(mode, w, d)
+    assert rq().rmsq_device_status() == 0
