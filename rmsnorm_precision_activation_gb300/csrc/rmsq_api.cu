@@ -291,10 +291,19 @@ static bool make_plan(int mode, int dt, bool res, bool w16, int hidden, const De
         if (best != 0) {
             const int nvc = nv / best;
             const long long cstage = static_cast<long long>(nvc) * 16 * (res ? 2 : 1);
-            int cv = 4;
-            while (cv < 8 && nvc > 256 * cv) cv *= 2;
-            // ring slots, reduction area, per slot an mbarrier and a row number, exchange slots
+            int cv = g_tune_vpt.load();
+            if (cv < 4 || (nvc + cv - 1) / cv > 512) {        // instantiated for 4 and 8
+                cv = 4;
+                while (cv < 8 && nvc > 256 * cv) cv *= 2;
+            }
+            // ring slots, reduction area, per slot an mbarrier and a row number, exchange slots.
+            // Kernels with one exchange per row (all but FP8 with an offset or fp32 input) hold
+            // two rows while their exchange is in flight, so a third slot keeps a load going:
+            // measured on GB300, 8-25 % faster than two slots at 16384-131072 elements, except
+            // FP8 in clusters of 16 (131072), where two slots are faster.
+            const bool one_exchange = mode != MODE_FP8 || w16;
             int stages = g_tune_stages.load();
+            if (stages == 0) stages = one_exchange && !(mode == MODE_FP8 && best == 16) ? 3 : 2;
             if (stages < 2) stages = 2;
             auto cbytes = [&](int st) { return st * cstage + red_bytes + st * 16 + kClusterXchBytes; };
             while (stages > 2 && cbytes(stages) > di.smem_optin) --stages;

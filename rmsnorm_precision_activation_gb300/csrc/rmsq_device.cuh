@@ -158,6 +158,18 @@ __device__ __forceinline__ void cluster_sync()
     asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
 }
 
+// The two halves of cluster_sync, for work placed between them. Every thread of every CTA calls
+// them alternately, arrive first.
+__device__ __forceinline__ void cluster_arrive()
+{
+    asm volatile("barrier.cluster.arrive.release;" ::: "memory");
+}
+
+__device__ __forceinline__ void cluster_wait()
+{
+    asm volatile("barrier.cluster.wait.acquire;" ::: "memory");
+}
+
 // Read a float4 at shared address `addr` of the CTA with cluster rank `rank`.
 __device__ __forceinline__ float4 ld_cluster_f4(uint32_t addr, uint32_t rank)
 {
@@ -704,10 +716,11 @@ struct GammaRegs<E, VPT, false> {
 // maxima, [128] NVFP4 element factors gs / dec(s) indexed by the E4M3 block-scale code (the
 // row-per-warp schedule reduces in registers and keeps only the factor table), then per ring
 // [stages] mbarriers and [stages] row numbers of the slots, then (SCHED_CLUSTER) the cluster
-// exchange slots: [2] float4 {sum hi, sum lo, max, stop} and [2] float4 {amax, -, -, -}.
+// exchange slots: [3] float4 {sum hi, sum lo, max, stop}, used in turn, and [2] float4
+// {amax, -, -, -}.
 constexpr int kRedFloats = 2 * 32 * 2 + 2 * 32 + 128;
 constexpr int kRedFloatsWarp = 128;
-constexpr int kClusterXchBytes = 4 * 16;
+constexpr int kClusterXchBytes = 5 * 16;
 
 // ------------------------------------------------------------------------------------------
 // The kernel
@@ -746,6 +759,9 @@ rmsq_row_kernel(const Params p)
     // and its store happen once per block and the codes leave in one 8-byte store.
     constexpr bool NV_BLOCKED = MODE == MODE_NVFP4 && RING && VPT >= GROUP;
     constexpr bool KEEP_Y = VPT <= 4 && !ONE_BAR && !SMEM_S;
+    // SCHED_CLUSTER with one exchange per row (every kernel that keeps s in its slot): the
+    // exchange of a row overlaps the first pass of the next one (see the row loop).
+    constexpr bool PIPE_X = CLUSTER && SMEM_S;
 
     extern __shared__ __align__(128) unsigned char smem[];
 
@@ -900,17 +916,24 @@ rmsq_row_kernel(const Params p)
     const float inv_h = __frcp_rn(Hf);
 
     float run_max = 0.0f;   // MODE_AMAX: max |y| over this thread's share of the CTA's rows
-    int stage = 0;          // ring slot of this row, and the mbarrier phase parity to wait for
+    int stage = 0;          // the next ring slot to wait on, and its mbarrier phase parity
     uint32_t parity = 0;
     int rbuf = 0;           // which of the two sum-of-squares reduction buffers this row uses
     bool aborted = false;   // a bounded wait ran out
-    int cpar = 0;           // SCHED_CLUSTER: which of the two sum exchange slots this row uses
-    int mpar = 0;           // SCHED_CLUSTER: the same for the FP8 row amax
+    int cslot = 0;          // SCHED_CLUSTER: which of the three sum exchange slots this row posts to
+    int mpar = 0;           // SCHED_CLUSTER: which of the two FP8 row amax slots this row uses
+    // PIPE_X: the row whose exchange is in flight (-1: none), its ring slot, slot address and
+    // exchange slot
+    long long pend_row = -1;
+    int pend_stage = 0;
+    uint32_t pend_addr = 0;
+    int pend_cslot = 0;
     long long reg_row = row0;
     for (;;) {
         // ---- which row: the slot's (ring schedules) or the next round-robin one --------------
         bool timed_out = false;
         uint32_t stage_addr = 0;
+        const int cur_stage = stage;  // the slot acquired here (PIPE_X: the ring moves on at once)
         long long row;
         if constexpr (RING) {
             stage_addr = smem_u32(ring + static_cast<size_t>(stage) * stage_bytes);
@@ -918,14 +941,22 @@ rmsq_row_kernel(const Params p)
             // The slot's row number was written before its barrier was armed, and an empty slot
             // (-1) completes at once, so every thread of the ring reads the same value here.
             row = slot_rows[stage];
-            if (row < 0) break;           // the ring handed out its last row
+            if constexpr (PIPE_X) {
+                if (++stage == S) {
+                    stage = 0;
+                    parity ^= 1u;
+                }
+            }
+            // the ring handed out its last row (PIPE_X: once the row in flight is finished)
+            if (row < 0 && (!PIPE_X || pend_row < 0)) break;
         } else {
             row = reg_row;
             reg_row += rstep;
             if (row >= p.rows) break;
         }
-        // false only after a timed-out wait; the loop then stops after the reduction's barrier
-        const bool have = !timed_out;
+        // false after a timed-out wait (the loop then stops after the exchange that reports it)
+        // and for the empty slot that ends a PIPE_X ring
+        const bool have = PIPE_X ? !timed_out && row >= 0 : !timed_out;
         const uint4* __restrict__ xrow = xg + row * stride;
         const uint4* __restrict__ rrow = RES ? rg + row * stride : nullptr;
         // ---- load the row, add the residual, write residual_output, sum of squares ----------
@@ -1045,41 +1076,91 @@ rmsq_row_kernel(const Params p)
                 tot = FF{__shfl_sync(0xFFFFFFFFu, t, 0), 0.0f};
             }
         }
+        // the row finished below and its ring slot: this row, or (PIPE_X) the one posted last time
+        int fin_stage = PIPE_X ? cur_stage : stage;
         if constexpr (CLUSTER) {
             // The cluster's CTAs trade their slice totals (and whether any wait ran out): each
-            // writes its own slot, one cluster barrier, then every CTA adds the C slots in rank
-            // order, so all of them hold the same row totals and take the same branch below.
-            float4* slot = &xch[cpar];
-            cpar ^= 1;
-            if (tid == 0) *slot = make_float4(tot.hi, tot.lo, tmax, stop ? 1.0f : 0.0f);
-            cluster_sync();
-            FF sum{0.0f, 0.0f};
-            float mx = 0.0f;
-            bool any = false;
-            for (uint32_t k = 0; k < csize; ++k) {
-                const float4 v = ld_cluster_f4(smem_u32(slot), k);
-                if constexpr (EXACT) sum = ff_add(sum, FF{v.x, v.y});
-                else sum.hi = __fadd_rn(sum.hi, v.x);
-                mx = fmaxf(mx, v.z);
-                any = any || v.w != 0.0f;
+            // writes its own slot, passes the cluster barrier, then every CTA adds the C slots in
+            // rank order, so all of them hold the same row totals and take the same branch below.
+            float4* slot = &xch[cslot];
+            const int my_cslot = cslot;
+            if (++cslot == 3) cslot = 0;
+            auto gather = [&](const float4* sl) {
+                FF sum{0.0f, 0.0f};
+                float mx = 0.0f;
+                bool any = false;
+                for (uint32_t k = 0; k < csize; ++k) {
+                    const float4 v = ld_cluster_f4(smem_u32(sl), k);
+                    if constexpr (EXACT) sum = ff_add(sum, FF{v.x, v.y});
+                    else sum.hi = __fadd_rn(sum.hi, v.x);
+                    mx = fmaxf(mx, v.z);
+                    any = any || v.w != 0.0f;
+                }
+                tot = sum;
+                tmax = mx;
+                stop = any;
+            };
+            if constexpr (PIPE_X) {
+                // Row i posts its totals, waits for the exchange of row i - 1 (posted one
+                // iteration ago, so its barrier had this row's first pass to complete), arrives
+                // for row i, then finishes row i - 1. Every CTA of the cluster walks the same rows
+                // and so makes the same barrier calls: arrive(0), wait(0) arrive(1), ...,
+                // wait(n - 1), then the final barrier. A slot is rewritten three rows later, after
+                // a barrier that every CTA passed only once done reading it.
+                const bool post = row >= 0;
+                if (post && tid == 0) *slot = make_float4(tot.hi, tot.lo, tmax, stop ? 1.0f : 0.0f);
+                if (pend_row < 0) {
+                    // the first row: nothing to finish yet
+                    cluster_arrive();
+                    pend_row = row;
+                    pend_stage = cur_stage;
+                    pend_addr = stage_addr;
+                    pend_cslot = my_cslot;
+                    continue;
+                }
+                cluster_wait();
+                gather(&xch[pend_cslot]);
+                if (post && !stop) cluster_arrive();
+                fin_stage = pend_stage;
+                const long long next_row_id = row;
+                const uint32_t next_addr = stage_addr;
+                row = pend_row;
+                stage_addr = pend_addr;
+                pend_row = next_row_id;
+                pend_stage = cur_stage;
+                pend_addr = next_addr;
+                pend_cslot = my_cslot;
+            } else {
+                if (tid == 0) *slot = make_float4(tot.hi, tot.lo, tmax, stop ? 1.0f : 0.0f);
+                cluster_sync();
+                gather(slot);
             }
-            tot = sum;
-            tmax = mx;
-            stop = any;
         }
         if (stop) {
             if constexpr (RING) {
                 if (issuer) {
                     atomicOr(p.err, ERRF_WAIT_TIMEOUT);
-                    // let the copies already issued into the other slots land (bounded)
+                    // Let the copies already issued into the ring's other slots land (bounded):
+                    // all after this row's slot, or (PIPE_X, where the ring has already moved
+                    // past the two rows held) all after the slot acquired last.
                     int js = stage;
                     uint32_t jp = parity;
-                    for (int j = 1; j < S; ++j) {
-                        if (++js == S) {
-                            js = 0;
-                            jp ^= 1u;
+                    if constexpr (PIPE_X) {
+                        for (int j = 0; j < S - 2; ++j) {
+                            mbar_wait_bounded(smem_u32(&bars[js]), jp, p.timeout_ns);
+                            if (++js == S) {
+                                js = 0;
+                                jp ^= 1u;
+                            }
                         }
-                        mbar_wait_bounded(smem_u32(&bars[js]), jp, p.timeout_ns);
+                    } else {
+                        for (int j = 1; j < S; ++j) {
+                            if (++js == S) {
+                                js = 0;
+                                jp ^= 1u;
+                            }
+                            mbar_wait_bounded(smem_u32(&bars[js]), jp, p.timeout_ns);
+                        }
                     }
                 }
             }
@@ -1089,7 +1170,7 @@ rmsq_row_kernel(const Params p)
         if constexpr (RING && !SMEM_S) {
             // Every thread has read this slot (s is held in registers): refill it now.
             if constexpr (WARP_ROWS) __syncwarp();
-            if (issuer) refill(stage, stage_addr, true);
+            if (issuer) refill(fin_stage, stage_addr, true);
         }
         float rstd;
         if constexpr (EXACT)
@@ -1174,7 +1255,7 @@ rmsq_row_kernel(const Params p)
                     amax = __shfl_sync(0xFFFFFFFFu, amax, 0);
                 }
                 if constexpr (CLUSTER) {
-                    float4* slot = &xch[2 + mpar];
+                    float4* slot = &xch[3 + mpar];
                     mpar ^= 1;
                     if (tid == 0) *slot = make_float4(amax, 0.0f, 0.0f, 0.0f);
                     cluster_sync();
@@ -1433,9 +1514,11 @@ rmsq_row_kernel(const Params p)
             } else {
                 __syncthreads();
             }
-            if (issuer) refill(stage, stage_addr, true);
+            if (issuer) refill(fin_stage, stage_addr, true);
         }
-        if constexpr (RING) {
+        if constexpr (PIPE_X) {
+            if (pend_row < 0) break;      // the row just finished was the last
+        } else if constexpr (RING) {
             if (++stage == S) {
                 stage = 0;
                 parity ^= 1u;
