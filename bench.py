@@ -767,7 +767,11 @@ def run_report_next(args):
                                                   epsilon=w.eps, swizzled=sw)
         return lambda: rq.rmsnorm_quant_mxfp4(x, g, residual=r, epsilon=w.eps, swizzled=sw)
 
+    only = set(args.only.split(",")) if args.only else None
     for row, case, w, opts in next_row_cases():
+        key = "%s:%s:%d:%d" % (case, w.mode, w.rows, w.hidden)
+        if only and case not in only and key not in only:
+            continue
         d = W.generate(w, seed=0, device="cuda")
         if "dtype" in opts:
             d = {k: (None if v is None else v.to(opts["dtype"])) for k, v in d.items()}
@@ -866,7 +870,8 @@ def main():
                     help="time the widened rows (swizzled scales, global-scale pre-pass, other "
                          "dtypes, cluster rows), one JSON line each")
     ap.add_argument("--only", default="", help="--report: comma-separated workload names "
-                    "(or name:rows:hidden for one MXFP4 sweep point)")
+                    "(or name:rows:hidden for one MXFP4 sweep point); --report-next: case names "
+                    "(or case:mode:rows:hidden)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-pdl", action="store_true",
                     help="launch without programmatic dependent launch (for comparison)")

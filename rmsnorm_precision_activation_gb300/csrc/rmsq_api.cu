@@ -288,6 +288,13 @@ static bool make_plan(int mode, int dt, bool res, bool w16, int hidden, const De
                 break;
             }
         }
+        const bool one_exchange = mode != MODE_FP8 || w16;
+        if (best == 16 && mode == MODE_FP8 && one_exchange && tune_c == 0 && nv % 8 == 0) {
+            // FP8 split 8 ways with a three-slot ring (one CTA per SM) measured faster on GB300
+            // than 16 ways (545 against 584-750 us at 2048 x 131072 with a residual)
+            const long long s8 = static_cast<long long>(nv / 8) * 16 * (res ? 2 : 1);
+            if (3 * s8 + red_bytes + 3 * 16 + kClusterXchBytes <= di.smem_optin) best = 8;
+        }
         if (best != 0) {
             const int nvc = nv / best;
             const long long cstage = static_cast<long long>(nvc) * 16 * (res ? 2 : 1);
@@ -299,11 +306,9 @@ static bool make_plan(int mode, int dt, bool res, bool w16, int hidden, const De
             // ring slots, reduction area, per slot an mbarrier and a row number, exchange slots.
             // Kernels with one exchange per row (all but FP8 with an offset or fp32 input) hold
             // two rows while their exchange is in flight, so a third slot keeps a load going:
-            // measured on GB300, 8-25 % faster than two slots at 16384-131072 elements, except
-            // FP8 in clusters of 16 (131072), where two slots are faster.
-            const bool one_exchange = mode != MODE_FP8 || w16;
+            // measured on GB300, 8-25 % faster than two slots at 16384-131072 elements.
             int stages = g_tune_stages.load();
-            if (stages == 0) stages = one_exchange && !(mode == MODE_FP8 && best == 16) ? 3 : 2;
+            if (stages == 0) stages = one_exchange ? 3 : 2;
             if (stages < 2) stages = 2;
             auto cbytes = [&](int st) { return st * cstage + red_bytes + st * 16 + kClusterXchBytes; };
             while (stages > 2 && cbytes(stages) > di.smem_optin) --stages;

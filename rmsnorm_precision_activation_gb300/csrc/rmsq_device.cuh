@@ -159,15 +159,18 @@ __device__ __forceinline__ void cluster_sync()
 }
 
 // The two halves of cluster_sync, for work placed between them. Every thread of every CTA calls
-// them alternately, arrive first.
-__device__ __forceinline__ void cluster_arrive()
-{
-    asm volatile("barrier.cluster.arrive.release;" ::: "memory");
-}
-
+// them alternately, arrive first. A thread whose earlier writes some other CTA reads after the
+// barrier arrives with release semantics (publish); any other thread arrives relaxed, without the
+// memory fence.
 __device__ __forceinline__ void cluster_wait()
 {
     asm volatile("barrier.cluster.wait.acquire;" ::: "memory");
+}
+
+__device__ __forceinline__ void cluster_arrive_as(bool publish)
+{
+    if (publish) asm volatile("barrier.cluster.arrive.release;" ::: "memory");
+    else asm volatile("barrier.cluster.arrive.relaxed;" ::: "memory");
 }
 
 // Read a float4 at shared address `addr` of the CTA with cluster rank `rank`.
@@ -1107,11 +1110,15 @@ rmsq_row_kernel(const Params p)
                 // and so makes the same barrier calls: arrive(0), wait(0) arrive(1), ...,
                 // wait(n - 1), then the final barrier. A slot is rewritten three rows later, after
                 // a barrier that every CTA passed only once done reading it.
+                // Only thread 0 writes what other CTAs read (the slot), so only it arrives with
+                // release semantics. The others arrive relaxed: their loads of the previous slots
+                // decide whether they arrive at all, so those loads are complete by then.
+                const bool publish = tid == 0;
                 const bool post = row >= 0;
                 if (post && tid == 0) *slot = make_float4(tot.hi, tot.lo, tmax, stop ? 1.0f : 0.0f);
                 if (pend_row < 0) {
                     // the first row: nothing to finish yet
-                    cluster_arrive();
+                    cluster_arrive_as(publish);
                     pend_row = row;
                     pend_stage = cur_stage;
                     pend_addr = stage_addr;
@@ -1120,7 +1127,7 @@ rmsq_row_kernel(const Params p)
                 }
                 cluster_wait();
                 gather(&xch[pend_cslot]);
-                if (post && !stop) cluster_arrive();
+                if (post && !stop) cluster_arrive_as(publish);
                 fin_stage = pend_stage;
                 const long long next_row_id = row;
                 const uint32_t next_addr = stage_addr;
