@@ -9,6 +9,8 @@ What each test would catch:
   fp8 quant         y / scale rounding                          -> torch float8_e4m3fn cast
   nvfp4 / mxfp4     block scale, element factor, nibble order   -> brute-force search per block
   invariants        |dequant - y| <= half a quantisation step (unclamped elements)
+  fp32 input        the fp32 sum rounded elsewhere, or y off    -> torch fp32 add, rms_norm (f64)
+  global scale      gs inverted or off by a factor             -> largest block scale is 448
 """
 import math
 
@@ -281,3 +283,42 @@ def test_fp8_rounded_scale_dtype(sdt, tdt):
     assert np.array_equal(low["scale"], want)
     assert np.allclose(low["pre"], low["y"].astype(np.float64) / want[:, None].astype(np.float64))
     assert np.array_equal(low["q"], oracle.e4m3_encode(low["pre"]))
+
+
+# ------------------------------------------------------------------------------------------
+# fp32 input and the NVFP4 global scale
+# ------------------------------------------------------------------------------------------
+
+def test_fp32_input_rows_match_torch():
+    # fp32 input: the residual sum is the fp32 sum itself, and y follows rms_norm in f64
+    rows, H = 16, 1024
+    gen = torch.Generator().manual_seed(11)
+    x = torch.randn(rows, H, generator=gen) * 2.0
+    r = torch.randn(rows, H, generator=gen)
+    g = torch.randn(H, generator=gen) * 0.1 + 1.0
+    out = oracle.quant_fp8(x.numpy(), r.numpy(), g.numpy(), dtype=oracle.F32, want_y=True)
+    s = x + r
+    assert np.array_equal(np.asarray(out["residual_output"]).view(np.uint32), s.numpy().view(np.uint32))
+    ref = F.rms_norm(s.double(), (H,), weight=g.double(), eps=float(np.float32(1e-6))).numpy()
+    y = out["y"].astype(np.float64)
+    assert np.all(np.abs(y - ref) <= 2.5 * 2.0 ** -24 * np.abs(ref) + 1e-30)
+
+
+def test_global_scale_puts_the_largest_block_on_448():
+    # gs maps the tensor's largest |y| onto the largest block scale (448) times the largest E2M1
+    # magnitude (6): the block holding it gets the E4M3 code of 448 and no block scale exceeds it
+    rows, H = 32, 512
+    x = _rand(rows, H, torch.bfloat16, 21, 1.0)
+    x[5, 77] = 40.0                                  # one outlier decides the tensor's max
+    g = (torch.randn(H, generator=torch.Generator().manual_seed(22)) * 0.1 + 1.0).to(torch.bfloat16)
+    y = oracle.rmsnorm(_bits(x), None, _bits(g))["y"]
+    r, c = np.unravel_index(np.argmax(np.abs(y)), y.shape)
+    gs = oracle.nvfp4_global_scale(np.abs(y).max())
+    out = oracle.quant_nvfp4(_bits(x), None, _bits(g), float(gs))
+    bs = out["block_scale"].reshape(rows, H // 16)
+    assert bs[r, c // 16] == 0x7E                    # 448
+    assert bs.max() == 0x7E
+    # the element at the max lands on E2M1 6 (code 7), with the sign of y
+    q = out["q"].reshape(rows, H // 2)[r, c // 2]
+    nib = (q >> (4 * (c % 2))) & 0xF
+    assert nib & 0x7 == 0x7 and (nib >> 3) == (1 if y[r, c] < 0 else 0)
