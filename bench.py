@@ -1,28 +1,34 @@
 """Benchmark of the fused residual-add + RMSNorm + FP8 / NVFP4 / MXFP4 path on GB300.
 
-One step is one pass of the whole hot path over one batch: the three quantisation modes, each on
-its own resident [8192 x 4096] bf16 batch with a residual (the fp8_residual workload's shape and
-distributions; FP8 with scale_ub 1200, NVFP4 with a device-computed global scale, MXFP4), so a
-step reads 384 MiB of inputs -- more than the 129 MB L2 -- and every launch streams from HBM.
+One step is one pass of the whole hot path over one batch of each of the three large workloads,
+at their stated shapes and distributions, each resident in HBM:
+  fp8    fp8_gemma        16384 x 8192 fp16 + residual, weight_offset 1, scale_ub 10
+  nvfp4  nvfp4            32768 x 7168 bf16, no residual, global scale from the device pre-pass
+                          (run once, before the timed region)
+  mxfp4  mxfp4_residual   65536 x 16384 bf16 + residual (the largest shape of the sweep)
+A step reads about 5 GB of distinct inputs -- far more than the 129 MB L2 -- so every launch
+streams from HBM and no flush is needed.
 
 Prints one JSON line:
-  value     whole-job GB/s of algorithmic bytes (each launch's reads + writes counted once),
-            inputs resident in HBM, CUDA-event timed over exactly K steps
-  e2e       the same metric through the public API with host buffers: pinned host -> device
-            copies of the step's inputs and device -> host copies of its outputs inside the
-            timed region, overlapped with the kernels on separate copy streams; beside it, the
-            same copies timed alone (the floor the host link sets)
-  roofline  the dominant kernel's achieved GB/s (its algorithmic bytes / its average launch time,
-            events on its launching stream around its launches in every 10th timed step,
-            from step 5 on)
-            against the measured HBM copy bandwidth; beside it, what a plain device copy of
-            the same bytes reaches
-  cpu_baseline  the oracle on a bounded sample of the same workload, on this host's cores
+  value      whole-job GB/s of algorithmic bytes (each launch's reads + writes counted once),
+             inputs resident in HBM, CUDA-event timed over exactly K steps
+  per_mode   each kernel's average launch time and GB/s (events on the launching stream around
+             its launches in every 5th timed step, from step 2 on)
+  rooflines  per kernel: those GB/s against the measured HBM copy bandwidth, the DRAM bytes of
+             one launch from the committed ncu capture (when taken on the current kernel
+             sources), and what a plain device copy of the same bytes reaches
+  roofline   the entry of the dominant kernel (the longest launch)
+  e2e        the same metric through the public API with host buffers: pinned host -> device
+             copies of the step's inputs and device -> host copies of its outputs inside the
+             timed region, overlapped with the kernels on separate copy streams; beside it, the
+             same copies timed alone (the floor the host link sets)
+  cpu_baseline  the oracle on a bounded row sample of the same three workloads, on this host's
+             cores
 
---impl reference times the oracle itself as the reference arm. --report runs every workload
-(fp8_small ... the MXFP4 sweep) and prints one JSON line per workload with its GB/s.
-Multi-GPU (torchrun): every rank runs an independent replica (the path has no exchange step);
-value is the sum of all ranks' bytes over the slowest rank's time.
+--impl reference times the oracle itself as the reference arm, on the same config. --report runs
+every workload (fp8_small ... the MXFP4 sweep) and prints one JSON line per workload with its
+GB/s. Multi-GPU (torchrun): every rank runs an independent replica (the path has no exchange
+step); value is the sum of all ranks' bytes over the slowest rank's time.
 """
 from __future__ import annotations
 
@@ -46,8 +52,17 @@ import workloads as W  # noqa: E402
 METRIC = "achieved HBM GB/s & rows/s, fused RMSNorm+FP8/FP4 quant, % of GB300 8 TB/s"
 NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
-STEP_SHAPE = (8192, 4096)
 MODES = ("fp8", "nvfp4", "mxfp4")
+# the step: one batch per quantisation mode, at the workload's stated shape
+STEP_WORKLOADS = {
+    "fp8": W.config("fp8_gemma"),
+    "nvfp4": W.config("nvfp4"),
+    "mxfp4": W.config("mxfp4_residual", rows=65536, hidden=16384),
+}
+KERNEL_NAMES = {"fp8": "rmsnorm_quant_fp8", "nvfp4": "rmsnorm_quant_nvfp4",
+                "mxfp4": "rmsnorm_quant_mxfp4"}
+# largest row sample of each workload the oracle is timed on (a fraction of its rows)
+ORACLE_MAX_FRACTION = 1.0 / 8
 
 
 # ------------------------------------------------------------------------------------------
@@ -80,9 +95,13 @@ def kernel_source_sha():
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(kernel):
-    """Per-launch DRAM bytes of `kernel` from the committed ncu summary, if it was taken on the
-    current kernel sources; else None."""
+def workload_label(w):
+    return "%s %dx%d" % (w.name, w.rows, w.hidden)
+
+
+def recorded_traffic(mode, w):
+    """Per-launch DRAM bytes (read + write) of the `mode` kernel on workload w from the committed
+    ncu summary, if it was taken on the current kernel sources and on that workload; else None."""
     path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
     try:
         with open(path) as f:
@@ -91,8 +110,10 @@ def recorded_traffic(kernel):
         return None
     if d.get("source_sha") != kernel_source_sha():
         return None
-    e = d.get("kernels", {}).get(kernel)
-    return None if e is None else e.get("dram_bytes_per_launch")
+    e = d.get("kernels", {}).get(mode)
+    if e is None or e.get("workload") != workload_label(w):
+        return None
+    return e.get("dram_bytes_per_launch")
 
 
 class ClockSampler:
@@ -150,9 +171,49 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
-def mode_bytes(mode, rows, hidden, residual=True):
-    name = {"fp8": "fp8_residual", "nvfp4": "nvfp4", "mxfp4": "mxfp4_residual"}[mode]
-    return W.Workload(name, mode, rows, hidden, "bf16", residual).algorithmic_bytes()
+def parse_step_workloads(spec):
+    """`mode=name[:rows:hidden],...` -> {mode: Workload}, over STEP_WORKLOADS (for experiments
+    on other shapes; the default step is STEP_WORKLOADS)."""
+    out = dict(STEP_WORKLOADS)
+    if not spec:
+        return out
+    out = {}
+    for item in spec.split(","):
+        mode, rest = item.split("=", 1)
+        parts = rest.split(":")
+        rows = int(parts[1]) if len(parts) > 1 else None
+        hidden = int(parts[2]) if len(parts) > 2 else None
+        w = W.config(parts[0], rows=rows, hidden=hidden)
+        if w.mode != mode:
+            raise SystemExit("workload %s is not a %s workload" % (parts[0], mode))
+        out[mode] = w
+    return out
+
+
+def step_config(workloads, world):
+    """The `config` object of the JSON line (identical in both arms)."""
+    inputs = sum(w.rows * w.hidden * 2 * (2 if w.residual else 1) for w in workloads.values())
+    desc = []
+    for m, w in workloads.items():
+        d = "%s %s %dx%d %s%s" % (m, w.name, w.rows, w.hidden, w.dtype,
+                                  " +residual" if w.residual else "")
+        if m == "fp8":
+            d += " offset %g ub %g" % (w.weight_offset, w.scale_ub)
+        desc.append(d)
+    return {
+        "workload": "fused residual-add + RMSNorm + quantisation, one batch per mode: "
+                    + "; ".join(desc),
+        "workloads": {m: {"name": w.name, "rows": w.rows, "hidden": w.hidden,
+                          "io_dtype": w.dtype, "residual": w.residual,
+                          "weight_offset": w.weight_offset,
+                          **({"scale_ub": w.scale_ub} if m == "fp8" else {}),
+                          **({"global_scale": "device pre-pass, before the timed region"}
+                             if m == "nvfp4" else {})}
+                      for m, w in workloads.items()},
+        "l2": "inputs larger than L2: %d MiB of distinct inputs per step, no flush"
+              % (inputs // (1 << 20)),
+        "parallelism": "replicas" if world > 1 else "single GPU",
+    }
 
 
 # ------------------------------------------------------------------------------------------
@@ -160,37 +221,43 @@ def mode_bytes(mode, rows, hidden, residual=True):
 # ------------------------------------------------------------------------------------------
 
 class Step:
-    """Resident buffers for one step: one batch per mode, outputs, and the launches."""
+    """Resident buffers for one step: one batch per mode at its workload's shape, outputs, the
+    NVFP4 global scale (device pre-pass, computed once here), and the launches."""
 
-    def __init__(self, rq, rows, hidden, device, seed=0):
+    def __init__(self, rq, device, workloads=None, seed=0):
         self.rq = rq
-        self.rows, self.hidden = rows, hidden
-        base = W.config("fp8_residual", rows=rows, hidden=hidden)
-        self.batches = {}
-        for k, mode in enumerate(MODES):
-            d = W.generate(base, seed=seed + k, device=device)
-            self.batches[mode] = d
-        self.w = base
+        self.workloads = dict(STEP_WORKLOADS if workloads is None else workloads)
+        self.batches, self.out = {}, {}
         dev = device
-        self.out = {
-            "fp8": (torch.empty(rows, hidden, dtype=torch.float8_e4m3fn, device=dev),
-                    torch.empty(rows, dtype=torch.float32, device=dev),
-                    torch.empty(rows, hidden, dtype=torch.bfloat16, device=dev)),
-            "nvfp4": (torch.empty(rows, hidden // 2, dtype=torch.uint8, device=dev),
-                      torch.empty(rows, hidden // 16, dtype=torch.float8_e4m3fn, device=dev),
-                      torch.empty(rows, hidden, dtype=torch.bfloat16, device=dev)),
-            "mxfp4": (torch.empty(rows, hidden // 2, dtype=torch.uint8, device=dev),
-                      torch.empty(rows, hidden // 32, dtype=torch.uint8, device=dev),
-                      torch.empty(rows, hidden, dtype=torch.bfloat16, device=dev)),
-        }
-        nb = self.batches["nvfp4"]
-        self.gs = rq.rmsnorm_nvfp4_global_scale(nb["input"], nb["gamma"], residual=nb["residual"],
-                                                epsilon=base.eps)
-        self.bytes = {m: mode_bytes(m, rows, hidden) for m in MODES}
+        for k, (mode, w) in enumerate(self.workloads.items()):
+            d = W.generate(w, seed=seed + k, device=dev)
+            self.batches[mode] = d
+            rows, hidden = w.rows, w.hidden
+            ro = torch.empty(rows, hidden, dtype=w.torch_dtype, device=dev) if w.residual else None
+            if mode == "fp8":
+                self.out[mode] = (torch.empty(rows, hidden, dtype=torch.float8_e4m3fn, device=dev),
+                                  torch.empty(rows, dtype=torch.float32, device=dev), ro)
+            elif mode == "nvfp4":
+                self.out[mode] = (torch.empty(rows, hidden // 2, dtype=torch.uint8, device=dev),
+                                  torch.empty(rows, hidden // 16, dtype=torch.float8_e4m3fn,
+                                              device=dev), ro)
+            else:
+                self.out[mode] = (torch.empty(rows, hidden // 2, dtype=torch.uint8, device=dev),
+                                  torch.empty(rows, hidden // 32, dtype=torch.uint8, device=dev),
+                                  ro)
+        self.gs = None
+        if "nvfp4" in self.workloads:
+            w, nb = self.workloads["nvfp4"], self.batches["nvfp4"]
+            self.gs = rq.rmsnorm_nvfp4_global_scale(nb["input"], nb["gamma"],
+                                                    residual=nb["residual"], epsilon=w.eps,
+                                                    weight_offset=w.weight_offset)
+        self.modes = tuple(self.workloads)
+        self.bytes = {m: w.algorithmic_bytes() for m, w in self.workloads.items()}
         self.step_bytes = sum(self.bytes.values())
+        self.step_rows = sum(w.rows for w in self.workloads.values())
 
     def launch(self, mode, stream=None):
-        d, o, w, rq = self.batches[mode], self.out[mode], self.w, self.rq
+        d, o, w, rq = self.batches[mode], self.out[mode], self.workloads[mode], self.rq
         if mode == "fp8":
             rq.rmsnorm_quant_fp8(d["input"], d["gamma"], residual=d["residual"], residual_output=o[2],
                                  epsilon=w.eps, weight_offset=w.weight_offset, scale_ub=w.scale_ub,
@@ -198,11 +265,13 @@ class Step:
         elif mode == "nvfp4":
             rq.rmsnorm_quant_nvfp4(d["input"], d["gamma"], global_scale=self.gs,
                                    residual=d["residual"], residual_output=o[2], epsilon=w.eps,
-                                   output=o[0], block_scale=o[1], stream=stream)
+                                   weight_offset=w.weight_offset, output=o[0], block_scale=o[1],
+                                   stream=stream)
         else:
             rq.rmsnorm_quant_mxfp4(d["input"], d["gamma"], residual=d["residual"],
-                                   residual_output=o[2], epsilon=w.eps, output=o[0],
-                                   block_scale=o[1], stream=stream)
+                                   residual_output=o[2], epsilon=w.eps,
+                                   weight_offset=w.weight_offset, output=o[0], block_scale=o[1],
+                                   stream=stream)
 
 
 def barrier_max(value, world):
@@ -227,8 +296,7 @@ def same_bytes_copy_gbs(nbytes, device, reps=10):
     """GB/s of a plain device-to-device copy that moves `nbytes` (half read, half written), the
     size of one launch. L2 is filled with clean lines by a 256 MiB read before each copy, so the
     copy reads from DRAM as the kernels do. Median of `reps` event-timed copies after 3
-    warm-ups. Reported beside the roofline: a launch of this size cannot run at the bandwidth of
-    the multi-GB copy the peak comes from, and this says what a copy reaches at the same size."""
+    warm-ups. Reported beside each roofline: what a copy reaches at the launch's size."""
     n = nbytes // 2 // 16 * 16
     src = torch.full((n,), 3, dtype=torch.uint8, device=device)
     dst = torch.empty_like(src)
@@ -243,6 +311,7 @@ def same_bytes_copy_gbs(nbytes, device, reps=10):
         torch.cuda.synchronize()
         if i >= 3:
             times.append(a.elapsed_time(b))
+    del src, dst, flush
     return 2 * n / statistics.median(times) / 1e6
 
 
@@ -250,6 +319,24 @@ def barrier(world):
     if world > 1:
         import torch.distributed as dist
         dist.barrier()
+
+
+def probed_steps(K):
+    """The timed steps whose launches get their own events: every 5th from step 2. An event
+    recorded between two kernels ends the programmatic overlap of the second with the first, so
+    the other steps run without them; the first steps are left out because the GPU can still be
+    waiting for the host there."""
+    return [i for i in range(K) if i % 5 == 2] or [K - 1]
+
+
+def roofline_entry(mode, w, us, peak, peak_src, copy_gbs):
+    gbs = w.algorithmic_bytes() / (us * 1e-6) / 1e9
+    return {"bound": "hbm", "kernel": KERNEL_NAMES[mode], "workload": workload_label(w),
+            "achieved": round(gbs, 1), "peak": peak,
+            "peak_source": peak_src + " (MEASURED_PEAKS hbm_gbs, copy)", "unit": "GB/s",
+            "frac": round(gbs / peak, 4), "traffic": recorded_traffic(mode, w),
+            "algorithmic_bytes_per_launch": w.algorithmic_bytes(), "us": round(us, 2),
+            "copy_same_bytes_gbs": round(copy_gbs, 1)}
 
 
 def run_ours(args):
@@ -265,25 +352,19 @@ def run_ours(args):
         rq.rmsq_set_pdl(False)
 
     device = torch.device("cuda", local)
-    rows, hidden = STEP_SHAPE
-    step = Step(rq, rows, hidden, device)
+    step = Step(rq, device, parse_step_workloads(args.step_workloads))
+    modes = step.modes
     stream = torch.cuda.current_stream(device)
 
     for _ in range(args.warmup):
-        for m in MODES:
+        for m in modes:
             step.launch(m)
     torch.cuda.synchronize()
 
     K = args.steps
-    # Per-kernel events go around the launches of every 10th step only (steps 5, 15, ...): an
-    # event recorded between two kernels ends the programmatic overlap of the second with the
-    # first (measured on GB300: 14 us of a 130 us step when every launch is bracketed), and the
-    # first steps are left out because the GPU can still be waiting for the host there. The
-    # step value comes from the events around all K steps; the kernel durations, from the
-    # bracketed launches, which lose that overlap and so read a little long.
-    probed = [i for i in range(K) if i % 10 == 5] or [K - 1]
+    probed = probed_steps(K)
     ev = {m: [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-              for _ in probed] for m in MODES}
+              for _ in probed] for m in modes}
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     launches0 = rq.rmsq_launch_count()
     barrier(world)
@@ -293,7 +374,7 @@ def run_ours(args):
         j = 0
         for i in range(K):
             probe = i in probed
-            for m in MODES:
+            for m in modes:
                 if probe:
                     ev[m][j][0].record(stream)
                 step.launch(m)
@@ -305,19 +386,23 @@ def run_ours(args):
     barrier(world)
     launches = rq.rmsq_launch_count() - launches0
     value, total_ms = replica_throughput(step.step_bytes, K, world, t0.elapsed_time(t1))
-    per_mode_ms = {m: statistics.mean(a.elapsed_time(b) for a, b in ev[m]) for m in MODES}
+    per_mode_ms = {m: statistics.mean(a.elapsed_time(b) for a, b in ev[m]) for m in modes}
     assert rq.rmsq_device_status() == 0
 
     # ---- end to end through the public API with host buffers -------------------------------
-    e2e = run_e2e(rq, step, device, max(3, min(K, 10)), world)
+    e2e = run_e2e(step, device, max(3, min(K, 10)), world)
 
-    rows_per_s = 3 * rows * K * world / (total_ms * 1e-3)
-    dom = max(per_mode_ms, key=per_mode_ms.get)
-    dom_gbs = step.bytes[dom] / (per_mode_ms[dom] * 1e-3) / 1e9
     peak, peak_src = measured_peak()
-    copy_gbs = same_bytes_copy_gbs(step.bytes[dom], device)
-    kname = {"fp8": "rmsnorm_quant_fp8", "nvfp4": "rmsnorm_quant_nvfp4",
-             "mxfp4": "rmsnorm_quant_mxfp4"}[dom]
+    rooflines = {}
+    for m in modes:
+        copy_gbs = same_bytes_copy_gbs(step.bytes[m], device)
+        rooflines[m] = roofline_entry(m, step.workloads[m], per_mode_ms[m] * 1e3, peak,
+                                      peak_src, copy_gbs)
+    dom = max(per_mode_ms, key=per_mode_ms.get)
+    roof = dict(rooflines[dom])
+    roof["timing"] = ("CUDA events on the launching stream around each launch of timed steps %s"
+                      % ",".join(str(i) for i in probed))
+    rows_per_s = step.step_rows * K * world / (total_ms * 1e-3)
     line = {
         "metric": METRIC,
         "value": round(value, 1),
@@ -330,35 +415,22 @@ def run_ours(args):
         "scaling": "weak",
         "vs_baseline": None,
         "dtype": "f32",
-        "data": "synthetic (seeded; workload fp8_residual distributions)",
-        "config": {
-            "workload": "fused residual-add + RMSNorm + {FP8 per-row, NVFP4, MXFP4} quantisation, "
-                        "one [8192 x 4096] bf16 batch with residual per mode",
-            "rows": rows, "hidden": hidden, "io_dtype": "bf16", "residual": True,
-            "modes": list(MODES), "fp8_scale_ub": 1200.0, "nvfp4_global_scale": "device pre-pass",
-            "l2": "inputs larger than L2: %d MiB of distinct inputs per step, no flush"
-                  % (3 * 2 * rows * hidden * 2 // (1 << 20)),
-            "parallelism": "replicas" if world > 1 else "single GPU",
-        },
+        "data": "synthetic (seeded; each workload's stated distributions)",
+        "config": step_config(step.workloads, world),
         "rows_per_s": round(rows_per_s),
         "pct_of_8tbs": round(100 * value / world / NOMINAL_HBM_GBS, 2),
-        "per_mode": {m: {"us": round(per_mode_ms[m] * 1e3, 2),
+        "per_mode": {m: {"workload": workload_label(step.workloads[m]),
+                         "us": round(per_mode_ms[m] * 1e3, 2),
                          "gbs": round(step.bytes[m] / (per_mode_ms[m] * 1e-3) / 1e9, 1),
-                         "algorithmic_bytes": step.bytes[m]} for m in MODES},
-        "roofline": {"bound": "hbm", "kernel": kname, "achieved": round(dom_gbs, 1),
-                     "peak": peak, "peak_source": peak_src + " (MEASURED_PEAKS hbm_gbs, copy)",
-                     "unit": "GB/s", "frac": round(dom_gbs / peak, 4),
-                     "traffic": recorded_traffic(kname),
-                     "timing": "CUDA events around each launch of timed steps %s"
-                               % ",".join(str(i) for i in probed),
-                     "algorithmic_bytes_per_launch": step.bytes[dom],
-                     "copy_same_bytes_gbs": round(copy_gbs, 1)},
+                         "algorithmic_bytes": step.bytes[m]} for m in modes},
+        "roofline": roof,
+        "rooflines": rooflines,
         "e2e": e2e,
         "gpu_launches": int(launches),
         "clocks": clocks.summary(),
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(seconds=args.cpu_seconds)
+        line["cpu_baseline"] = cpu_baseline(step.workloads, seconds=args.cpu_seconds)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -366,33 +438,44 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
-def run_e2e(rq, step, device, K, world):
+def run_e2e(step, device, K, world):
     """Same step through the public API, inputs from pinned host memory and outputs back to
     pinned host memory inside the timed region.
 
-    The three batches move through three streams, the way a caller overlaps transfers with
-    compute: one stream copies each batch's inputs in (pinned host -> device), the launch stream
-    runs the kernels, and one stream copies each batch's outputs back (device -> pinned host).
-    Events order each batch's copy-in, kernel and copy-out. They also stop a copy-in from
-    overwriting inputs that batch's previous kernel still reads, and a kernel from overwriting
-    outputs that are still being copied out."""
-    host_in = {m: {k: v.cpu().pin_memory() for k, v in step.batches[m].items() if v is not None}
-               for m in MODES}
-    host_out = {m: tuple(torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in step.out[m])
-                for m in MODES}
+    The batches move through three streams, the way a caller overlaps transfers with compute:
+    one stream copies each batch's inputs in (pinned host -> device), the launch stream runs the
+    kernels, and one stream copies each batch's outputs back (device -> pinned host). Events
+    order each batch's copy-in, kernel and copy-out. They also stop a copy-in from overwriting
+    inputs that batch's previous kernel still reads, and a kernel from overwriting outputs that
+    are still being copied out."""
+    modes = step.modes
+
+    def pinned_like(t):
+        return torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
+
+    host_in = {}
+    for m in modes:
+        host_in[m] = {}
+        for k, v in step.batches[m].items():
+            if v is not None:
+                h = pinned_like(v)
+                h.copy_(v)
+                host_in[m][k] = h
+    host_out = {m: tuple(pinned_like(t) for t in step.out[m] if t is not None) for m in modes}
+    dev_out = {m: tuple(t for t in step.out[m] if t is not None) for m in modes}
     h2d = sum(t.numel() * t.element_size() for d in host_in.values() for t in d.values())
     d2h = sum(t.numel() * t.element_size() for o in host_out.values() for t in o)
     compute = torch.cuda.current_stream(device)
     s_in, s_out = torch.cuda.Stream(device), torch.cuda.Stream(device)
-    in_done = {m: torch.cuda.Event() for m in MODES}
-    ker_done = {m: torch.cuda.Event() for m in MODES}
-    out_done = {m: torch.cuda.Event() for m in MODES}
-    for m in MODES:
+    in_done = {m: torch.cuda.Event() for m in modes}
+    ker_done = {m: torch.cuda.Event() for m in modes}
+    out_done = {m: torch.cuda.Event() for m in modes}
+    for m in modes:
         ker_done[m].record(compute)
         out_done[m].record(compute)
 
     def one():
-        for m in MODES:
+        for m in modes:
             s_in.wait_event(ker_done[m])
             with torch.cuda.stream(s_in):
                 for k, t in host_in[m].items():
@@ -404,7 +487,7 @@ def run_e2e(rq, step, device, K, world):
             ker_done[m].record(compute)
             s_out.wait_event(ker_done[m])
             with torch.cuda.stream(s_out):
-                for dst, src in zip(host_out[m], step.out[m]):
+                for dst, src in zip(host_out[m], dev_out[m]):
                     dst.copy_(src, non_blocking=True)
             out_done[m].record(s_out)
 
@@ -425,12 +508,12 @@ def run_e2e(rq, step, device, K, world):
     # The same copies with no kernels and no ordering between the two directions: the floor the
     # host link sets under the end-to-end step. Timed after the step, outside its timed region.
     def copies_only():
-        for m in MODES:
+        for m in modes:
             with torch.cuda.stream(s_in):
                 for k, t in host_in[m].items():
                     step.batches[m][k].copy_(t, non_blocking=True)
             with torch.cuda.stream(s_out):
-                for dst, src in zip(host_out[m], step.out[m]):
+                for dst, src in zip(host_out[m], dev_out[m]):
                     dst.copy_(src, non_blocking=True)
 
     copies_only()
@@ -446,6 +529,7 @@ def run_e2e(rq, step, device, K, world):
     c1.record(compute)
     torch.cuda.synchronize()
     copy_ms = c0.elapsed_time(c1) / K
+    del host_in, host_out
     return {"value": round(value, 1), "unit": "GB/s",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "ms_per_step": round(ms / K, 4), "steps": K,
@@ -457,44 +541,72 @@ def run_e2e(rq, step, device, K, world):
 # the oracle on the host cores
 # ------------------------------------------------------------------------------------------
 
-def oracle_sample(rows_per_mode, seed=0):
+def sample_workloads(workloads, fraction):
+    """The same workloads cut to `fraction` of their rows (at least one row each)."""
+    import dataclasses
+    return {m: dataclasses.replace(w, rows=max(1, int(round(w.rows * fraction))))
+            for m, w in workloads.items()}
+
+
+def oracle_sample(workloads, fraction, seed=0):
+    """A callable that runs the oracle, as it stands, over a `fraction` row sample of every
+    workload of the step (inputs drawn with the workloads' own recipes), and the sample's
+    algorithmic bytes and rows."""
     import numpy as np
     import oracle
-    rows, hidden = rows_per_mode, STEP_SHAPE[1]
-    base = W.config("fp8_residual", rows=rows, hidden=hidden)
-    data = {}
-    for k, m in enumerate(MODES):
-        d = W.generate(base, seed=seed + k)
-        data[m] = tuple(W.bits(d[n]) for n in ("input", "residual", "gamma"))
-    x, r, g = data["nvfp4"]
-    y = oracle.rmsnorm(x, r, g, eps=base.eps)["y"]
-    gs = float(oracle.nvfp4_global_scale(np.abs(y).max()))
+    sample = sample_workloads(workloads, fraction)
+    calls = []
+    for k, (m, w) in enumerate(sample.items()):
+        d = W.generate(w, seed=seed + k)
+        x, g = W.bits(d["input"]), W.bits(d["gamma"])
+        r = None if d["residual"] is None else W.bits(d["residual"])
+        odt = {"bf16": oracle.BF16, "fp16": oracle.FP16}[w.dtype]
+        kw = dict(dtype=odt, eps=w.eps, weight_offset=w.weight_offset)
+        if m == "fp8":
+            calls.append(lambda x=x, r=r, g=g, ub=w.scale_ub, kw=kw:
+                         oracle.quant_fp8(x, r, g, scale_ub=ub, **kw))
+        elif m == "nvfp4":
+            y = oracle.rmsnorm(x, r, g, **kw)["y"]
+            gs = float(oracle.nvfp4_global_scale(np.abs(y).max()))
+            calls.append(lambda x=x, r=r, g=g, gs=gs, kw=kw: oracle.quant_nvfp4(x, r, g, gs, **kw))
+        else:
+            calls.append(lambda x=x, r=r, g=g, kw=kw: oracle.quant_mxfp4(x, r, g, **kw))
 
-    def run(threads=None):
-        x, r, g = data["fp8"]
-        oracle.quant_fp8(x, r, g, eps=base.eps, scale_ub=base.scale_ub, threads=threads)
-        x, r, g = data["nvfp4"]
-        oracle.quant_nvfp4(x, r, g, gs, eps=base.eps, threads=threads)
-        x, r, g = data["mxfp4"]
-        oracle.quant_mxfp4(x, r, g, eps=base.eps, threads=threads)
+    def run():
+        for c in calls:
+            c()
 
-    nbytes = sum(mode_bytes(m, rows, hidden) for m in MODES)
-    return run, nbytes
+    nbytes = sum(w.algorithmic_bytes() for w in sample.values())
+    rows = sum(w.rows for w in sample.values())
+    return run, nbytes, rows, sample
 
 
-def cpu_baseline(seconds=15.0):
-    import oracle
-    oracle.build()
-    cores = oracle.cores()
-    probe_rows = 64
-    run, nb = oracle_sample(probe_rows)
+def describe_sample(sample):
+    return ", ".join("%s %d of %d rows" % (w.name, w.rows, STEP_ROWS.get(w.name, w.rows))
+                     for w in sample.values())
+
+
+STEP_ROWS = {w.name: w.rows for w in STEP_WORKLOADS.values()}
+
+
+def size_oracle_sample(workloads, seconds_per_pass):
+    """The row fraction whose oracle pass takes about `seconds_per_pass`, from a timed probe on a
+    small fraction; at most ORACLE_MAX_FRACTION."""
+    probe = 1.0 / 1024
+    run, nb, _, _ = oracle_sample(workloads, probe, seed=900)
     t = time.perf_counter()
     run()
     dt = max(time.perf_counter() - t, 1e-3)
-    rows = int(max(probe_rows, min(8192, probe_rows * seconds / dt / 2)))
-    run, nb = oracle_sample(rows, seed=100)
-    # Whole passes over the sample until about `seconds` of wall time: when the sample is the
-    # full step, one pass alone is too short to time well.
+    return min(ORACLE_MAX_FRACTION, probe * seconds_per_pass / dt)
+
+
+def cpu_baseline(workloads, seconds=15.0):
+    import oracle
+    oracle.build()
+    cores = oracle.cores()
+    frac = size_oracle_sample(workloads, seconds / 4)
+    run, nb, rows, sample = oracle_sample(workloads, frac, seed=100)
+    # Whole passes over the sample until about `seconds` of wall time.
     passes, dt = 0, 0.0
     while passes == 0 or dt < seconds:
         t = time.perf_counter()
@@ -503,9 +615,8 @@ def cpu_baseline(seconds=15.0):
         passes += 1
     return {"value": round(passes * nb / dt / 1e9, 4), "unit": "GB/s", "cores": cores,
             "kind": "oracle",
-            "sample": "%d pass(es) over %d rows x 4096 per mode (fp8 / nvfp4 / mxfp4, bf16 + "
-                      "residual), %.1f s" % (passes, rows, dt),
-            "rows_per_s": round(3 * rows * passes / dt, 1)}
+            "sample": "%d pass(es) over %s (%.1f s)" % (passes, describe_sample(sample), dt),
+            "rows_per_s": round(rows * passes / dt, 1)}
 
 
 def run_reference(args):
@@ -515,13 +626,10 @@ def run_reference(args):
     import oracle
     oracle.build()
     cores = oracle.cores()
-    budget = 120.0 / max(1, args.steps + args.warmup)      # whole run within ~2 minutes
-    run, nb = oracle_sample(64)
-    t = time.perf_counter()
-    run()
-    dt = max(time.perf_counter() - t, 1e-3)
-    rows = int(max(16, min(8192, 64 * budget / dt / 2)))
-    run, nb = oracle_sample(rows, seed=200)
+    workloads = parse_step_workloads(getattr(args, "step_workloads", ""))
+    budget = 100.0 / max(1, args.steps + args.warmup)      # whole run within about 2 minutes
+    frac = size_oracle_sample(workloads, budget)
+    run, nb, rows, sample = oracle_sample(workloads, frac, seed=200)
     for _ in range(args.warmup):
         run()
     times = []
@@ -536,15 +644,12 @@ def run_reference(args):
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(total / args.steps * 1e3, 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic (seeded; workload fp8_residual distributions)",
-        "config": {"workload": "fused residual-add + RMSNorm + {FP8 per-row, NVFP4, MXFP4} "
-                               "quantisation, one [8192 x 4096] bf16 batch with residual per mode",
-                   "rows": STEP_SHAPE[0], "hidden": STEP_SHAPE[1], "io_dtype": "bf16",
-                   "residual": True, "modes": list(MODES),
-                   "sample_rows_per_mode": rows},
+        "data": "synthetic (seeded; each workload's stated distributions)",
+        "config": step_config(workloads, world),
+        "rows_per_s": round(rows * args.steps / total, 1),
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": cores,
                          "kind": "oracle",
-                         "sample": "%d of 8192 rows per mode per step" % rows},
+                         "sample": "each step one pass over %s" % describe_sample(sample)},
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
@@ -872,6 +977,9 @@ def main():
     ap.add_argument("--only", default="", help="--report: comma-separated workload names "
                     "(or name:rows:hidden for one MXFP4 sweep point); --report-next: case names "
                     "(or case:mode:rows:hidden)")
+    ap.add_argument("--step-workloads", default="",
+                    help="replace the step's batches: mode=name[:rows:hidden],... (experiments; "
+                         "the default is the three large workloads)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-pdl", action="store_true",
                     help="launch without programmatic dependent launch (for comparison)")

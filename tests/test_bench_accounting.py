@@ -44,10 +44,42 @@ def test_workload_bytes(name, rows, hidden, value):
     assert value == _expected(w.mode, w.rows, w.hidden, 2, w.residual)
 
 
-def test_bench_step_bytes_are_the_three_launches():
-    total = sum(bench.mode_bytes(m, 8192, 4096) for m in bench.MODES)
-    assert total == sum(_expected(m, 8192, 4096, 2, True) for m in bench.MODES)
-    assert bench.mode_bytes("fp8", 8192, 4096) == 234_921_984
+def test_bench_step_is_the_three_large_workloads():
+    # the step times each mode on its large workload at the stated shape
+    st = bench.STEP_WORKLOADS
+    assert (st["fp8"].name, st["fp8"].rows, st["fp8"].hidden, st["fp8"].dtype) == \
+        ("fp8_gemma", 16384, 8192, "fp16")
+    assert st["fp8"].residual and st["fp8"].weight_offset == 1.0 and st["fp8"].scale_ub == 10.0
+    assert (st["nvfp4"].name, st["nvfp4"].rows, st["nvfp4"].hidden, st["nvfp4"].residual) == \
+        ("nvfp4", 32768, 7168, False)
+    assert (st["mxfp4"].name, st["mxfp4"].rows, st["mxfp4"].hidden, st["mxfp4"].residual) == \
+        ("mxfp4_residual", 65536, 16384, True)
+    total = sum(w.algorithmic_bytes() for w in st.values())
+    assert total == 939_606_016 + 601_896_964 + 7_012_909_056
+    assert total == sum(_expected(w.mode, w.rows, w.hidden, 2, w.residual) for w in st.values())
+
+
+def test_both_arms_report_the_same_config():
+    # the reference arm's line carries the config of the step it stands beside
+    a = bench.step_config(bench.STEP_WORKLOADS, 1)
+    b = bench.step_config(bench.parse_step_workloads(""), 1)
+    assert a == b
+    assert "fp8_gemma 16384x8192 fp16 +residual offset 1 ub 10" in a["workload"]
+    assert "mxfp4_residual 65536x16384 bf16 +residual" in a["workload"]
+    # about 5 GB of distinct inputs per step: no L2 flush needed
+    assert "no flush" in a["l2"] and int(a["l2"].split()[4]) > 4000
+
+
+def test_step_override_and_oracle_sample_sizes():
+    ws = bench.parse_step_workloads("fp8=fp8_residual,mxfp4=mxfp4_residual:4096:2048")
+    assert list(ws) == ["fp8", "mxfp4"] and ws["mxfp4"].rows == 4096
+    with pytest.raises(SystemExit):
+        bench.parse_step_workloads("fp8=nvfp4")
+    s = bench.sample_workloads(bench.STEP_WORKLOADS, 1.0 / 8)
+    assert [w.rows for w in s.values()] == [2048, 4096, 8192]
+    assert all(w.hidden == bench.STEP_WORKLOADS[m].hidden for m, w in s.items())
+    tiny = bench.sample_workloads(bench.STEP_WORKLOADS, 1e-9)
+    assert all(w.rows == 1 for w in tiny.values())
 
 
 @pytest.mark.parametrize("case", bench.next_row_cases(), ids=lambda c: "%s-%s-%dx%d" % (

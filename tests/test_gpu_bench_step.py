@@ -1,12 +1,13 @@
 """The launches bench.py times, checked against the oracle.
 
-bench.py's step runs the FP8, NVFP4 and MXFP4 kernels on three resident [8192 x 4096] bf16
-batches with a residual. It uses the fp8_residual workload's distributions, FP8 with
-scale_ub 1200, and NVFP4 with the global scale from the device pre-pass. This test builds that
-same Step, runs its launches back to back on one stream as the timed loop does (twice, so the
-second pass reuses the buffers and counters), and checks sampled rows of every output against
-the oracle. The device global scale is compared with the oracle's amax, then used as the
-oracle's input for the NVFP4 codes."""
+bench.py's step runs the FP8, NVFP4 and MXFP4 kernels, each on its large workload at the stated
+shape: fp8_gemma (16384 x 8192 fp16 + residual, weight_offset 1, scale_ub 10), nvfp4
+(32768 x 7168 bf16, global scale from the device pre-pass) and mxfp4_residual at
+65536 x 16384. This test builds that same Step, runs its launches back to back on one stream as
+the timed loop does (twice, so the second pass reuses the buffers and row counters), and checks
+sampled rows of every output against the oracle. The device global scale is compared with the
+oracle's, computed over the whole nvfp4 tensor, then used as the oracle's input for the NVFP4
+codes."""
 import numpy as np
 import pytest
 import torch
@@ -21,46 +22,56 @@ pytestmark = pytest.mark.gpu
 def test_bench_step_launches_match_oracle():
     import bench
     dev = torch.device("cuda", 0)
-    step = bench.Step(rq(), 8192, 4096, dev)
+    step = bench.Step(rq(), dev)
+    assert step.modes == ("fp8", "nvfp4", "mxfp4")
     for _ in range(2):
-        for m in bench.MODES:
+        for m in step.modes:
             step.launch(m)
     torch.cuda.synchronize()
-    w = step.w
-    idx = sample_rows(8192, 48, seed=17)
-    t_idx = torch.as_tensor(idx, device=dev)
 
-    def rows(t):
-        return None if t is None else t[t_idx]
+    def rows_of(t, idx):
+        return None if t is None else t[torch.as_tensor(idx, device=dev)]
 
-    # FP8
-    d = step.batches["fp8"]
+    def bits(t, idx):
+        return None if t is None else host_bits(rows_of(t, idx))
+
+    # FP8 on fp8_gemma, with the rows whose input was scaled x200 among the samples
+    w, d = step.workloads["fp8"], step.batches["fp8"]
+    big = torch.nonzero(d["input"].float().abs().amax(-1) > 50).flatten().cpu().numpy()
+    assert len(big) > 50
+    idx = sample_rows(w.rows, 48, seed=17, extra=big[:16])
     q, sc, ro = step.out["fp8"]
-    ora = oracle.quant_fp8(host_bits(rows(d["input"])), host_bits(rows(d["residual"])),
-                           host_bits(d["gamma"]), dtype=ODT[torch.bfloat16], eps=w.eps,
+    ora = oracle.quant_fp8(bits(d["input"], idx), bits(d["residual"], idx), host_bits(d["gamma"]),
+                           dtype=ODT[d["input"].dtype], eps=w.eps,
                            weight_offset=w.weight_offset, scale_ub=w.scale_ub, want_pre=True)
-    P.compare_fp8(rows(q.view(torch.uint8)).cpu().numpy(), rows(sc).cpu().numpy(),
-                  host_bits(rows(ro)), ora).check()
+    rep = P.compare_fp8(rows_of(q.view(torch.uint8), idx).cpu().numpy(),
+                        rows_of(sc, idx).cpu().numpy(), bits(ro, idx), ora).check()
+    assert rep["bad"] == 0
 
     # NVFP4 with the device global scale
-    d = step.batches["nvfp4"]
+    w, d = step.workloads["nvfp4"], step.batches["nvfp4"]
     gs = float(step.gs.cpu()[0])
-    y = oracle.rmsnorm(host_bits(d["input"]), host_bits(d["residual"]), host_bits(d["gamma"]),
-                       dtype=ODT[torch.bfloat16], eps=w.eps)["y"]
+    y = oracle.rmsnorm(host_bits(d["input"]), None, host_bits(d["gamma"]),
+                       dtype=ODT[d["input"].dtype], eps=w.eps)["y"]
     gs_ora = float(oracle.nvfp4_global_scale(np.abs(y).max()))
+    del y
     assert abs(gs - gs_ora) <= 2e-6 * gs_ora, (gs, gs_ora)
+    idx = sample_rows(w.rows, 48, seed=18)
     q, bs, ro = step.out["nvfp4"]
-    ora = oracle.quant_nvfp4(host_bits(rows(d["input"])), host_bits(rows(d["residual"])),
-                             host_bits(d["gamma"]), gs, dtype=ODT[torch.bfloat16], eps=w.eps,
-                             want_y=True, want_pre=True)
-    P.compare_nvfp4(rows(q).cpu().numpy(), rows(bs.view(torch.uint8)).cpu().numpy(),
-                    host_bits(rows(ro)), ora, gs).check()
+    assert ro is None
+    ora = oracle.quant_nvfp4(bits(d["input"], idx), None, host_bits(d["gamma"]), gs,
+                             dtype=ODT[d["input"].dtype], eps=w.eps, want_y=True, want_pre=True)
+    P.compare_nvfp4(rows_of(q, idx).cpu().numpy(), rows_of(bs.view(torch.uint8), idx).cpu().numpy(),
+                    None, ora, gs).check()
 
-    # MXFP4
-    d = step.batches["mxfp4"]
+    # MXFP4 at 65536 x 16384
+    w, d = step.workloads["mxfp4"], step.batches["mxfp4"]
+    idx = sample_rows(w.rows, 32, seed=19)
     q, bs, ro = step.out["mxfp4"]
-    ora = oracle.quant_mxfp4(host_bits(rows(d["input"])), host_bits(rows(d["residual"])),
-                             host_bits(d["gamma"]), dtype=ODT[torch.bfloat16], eps=w.eps,
-                             want_y=True, want_pre=True)
-    P.compare_mxfp4(rows(q).cpu().numpy(), rows(bs).cpu().numpy(), host_bits(rows(ro)), ora).check()
+    ora = oracle.quant_mxfp4(bits(d["input"], idx), bits(d["residual"], idx), host_bits(d["gamma"]),
+                             dtype=ODT[d["input"].dtype], eps=w.eps, want_y=True, want_pre=True)
+    P.compare_mxfp4(rows_of(q, idx).cpu().numpy(), rows_of(bs, idx).cpu().numpy(),
+                    bits(ro, idx), ora).check()
+    del step
+    torch.cuda.empty_cache()
     assert rq().rmsq_device_status() == 0
