@@ -44,6 +44,8 @@ struct DeviceInfo {
     bool usable = false;
     int sms = 0;
     int smem_optin = 0;
+    int smem_per_sm = 0;       // shared memory of one SM
+    int smem_reserved = 0;     // shared memory the system reserves per CTA
     unsigned int* err = nullptr;
     unsigned int* counters = nullptr;
 };
@@ -68,6 +70,10 @@ static const DeviceInfo* device_info()
                   cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) == cudaSuccess &&
                   cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess &&
                   cudaDeviceGetAttribute(&d.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) ==
+                      cudaSuccess &&
+                  cudaDeviceGetAttribute(&d.smem_per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) ==
+                      cudaSuccess &&
+                  cudaDeviceGetAttribute(&d.smem_reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev) ==
                       cudaSuccess;
         void* addr = nullptr;
         void* ctr = nullptr;
@@ -354,7 +360,33 @@ static bool make_plan(int mode, int dt, bool res, bool w16, int hidden, const De
         else if (!res) pl.ctas_per_sm = 8;
         else pl.ctas_per_sm = 8;
     }
-    if (pl.sched == SCHED_PIPE) {
+    // The FP8 kernel with a weight offset and 16-bit input (four vectors per thread) keeps w in
+    // a shared-memory table of 32 bytes per vector (at most 2048 vectors per row, so the table
+    // and one slot always fit). Its ring takes two slots when that costs no resident CTA, else
+    // one: measured on GB300, one slot is faster for rows of 4096 and 8192 (3 and 6 CTAs per SM
+    // instead of 2 and 4) and two for rows of 2048 and 16384, where the CTA count is the same.
+    const bool gamma_table = mode == MODE_FP8 && !w16 && dt != DT_F32 && vpt == 4 &&
+                             pl.sched == SCHED_PIPE;
+    if (gamma_table) {
+        const long long table = 32LL * nv;
+        auto bytes = [&](int st) { return st * stage + table + red_bytes + st * 16; };
+        // resident CTAs: the CTA cap, the kernel's register cap in 256-register warp units, and
+        // shared memory
+        auto ctas = [&](int st) {
+            long long c = pl.ctas_per_sm;
+            constexpr int regs = reg_cap<DT_FP16, MODE_FP8, 4, SCHED_PIPE, false>();
+            const long long by_regs = (65536 / (regs * 32)) / (threads / 32);
+            const long long by_smem = di.smem_per_sm / (bytes(st) + di.smem_reserved);
+            if (by_regs < c) c = by_regs;
+            if (by_smem < c) c = by_smem;
+            return c;
+        };
+        int stages = g_tune_stages.load();
+        if (stages == 0) stages = (bytes(2) <= di.smem_optin && ctas(2) >= ctas(1)) ? 2 : 1;
+        while (stages > 1 && bytes(stages) > di.smem_optin) --stages;
+        pl.stages = stages;
+        pl.smem = static_cast<int>(bytes(stages));
+    } else if (pl.sched == SCHED_PIPE) {
         int stages = g_tune_stages.load();
         if (stages == 0)
             stages = (mode != MODE_FP8 && res && ((nv >= 256 && nv < 512) || nv >= 2048)) ? 3 : 2;

@@ -33,6 +33,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <type_traits>
+
 namespace rmsq {
 
 enum { DT_BF16 = 0, DT_FP16 = 1, DT_F32 = 2 };
@@ -504,6 +506,15 @@ __device__ __forceinline__ float warp_max(float v)
     return v;
 }
 
+// max |v| over the 32 lanes of a full warp, in one warp-wide reduction instruction (every lane
+// gets the result). For the non-negative finite values the kernels reduce, it equals warp_max.
+__device__ __forceinline__ float warp_max_abs(float v)
+{
+    float r;
+    asm volatile("redux.sync.max.abs.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(v));
+    return r;
+}
+
 // UE8M0 code of a block with max |y| = a >= 0: the smallest e with 6 * 2^e >= a, plus 127,
 // clamped to [0, 255]; 0 for a = 0. Exact, from a's bits: for a = m * 2^E with m in [1, 2),
 // a / 6 <= 2^(E-2) exactly when m <= 1.5, so e = E - 2 if m <= 1.5 and E - 1 otherwise.
@@ -572,6 +583,16 @@ __device__ __forceinline__ void two_sum2(float2 a, float2 b, float2& s, float2& 
     s = add2(a, b);
     const float2 bb = sub2(s, a);
     e = add2(sub2(a, sub2(s, bb)), sub2(b, bb));
+}
+
+// a + b for non-negative a.hi, b.hi (partial sums of squares): Fast2Sum on the larger and the
+// smaller high part gives the same exact split as TwoSum in fewer dependent steps.
+__device__ __forceinline__ FF ff_add_pos(FF a, FF b)
+{
+    const float big = fmaxf(a.hi, b.hi), small = fminf(a.hi, b.hi);
+    const float s = __fadd_rn(big, small);
+    const float e = __fsub_rn(small, __fsub_rn(s, big));
+    return FF{s, __fadd_rn(__fadd_rn(a.lo, b.lo), e)};
 }
 
 __device__ __forceinline__ FF shfl_xor_ff(FF v, int o)
@@ -715,12 +736,82 @@ struct GammaRegs<E, VPT, false> {
     }
 };
 
+// w for the FP8 kernels with a weight offset and 16-bit input: no registers held across the
+// row. Each use re-reads the thread's gamma vector (16 KB at most for a row of 8192, resident in
+// L1 for the kernel's lifetime) and adds the offset; those kernels use w once per row, and the
+// registers saved let three 256-thread CTAs share an SM.
+template <class E, int VPT>
+struct GammaL1 {
+    static constexpr int NP = E::EPV / 2;
+    const uint4* gp;
+    int tid, T, nv;
+    float2 off;
+    __device__ __forceinline__ void load(const uint4* g, int t, int TT, int n, float2 o, int = 1)
+    {
+        gp = g;
+        tid = t;
+        T = TT;
+        nv = n;
+        off = o;
+    }
+    __device__ __forceinline__ void get(int k, float2 (&out)[NP]) const
+    {
+        const int v = tid + k * T;
+        E::pairs(v < nv ? __ldg(gp + v) : make_uint4(0, 0, 0, 0), out);
+#pragma unroll
+        for (int j = 0; j < NP; ++j) out[j] = add2(out[j], off);
+    }
+};
+
+// w for the same kernels on the CTA-per-row ring, kept in shared memory as fp32 and formed once
+// per CTA: two planes of 16 bytes per vector (pairs 0-1, then pairs 2-3), so a warp's reads of
+// either plane are contiguous. The planner pays for the table with ring slots (one slot for rows
+// of 8192: measured on GB300, 138.9 us against 144.0 us with w re-read from L1 and two slots).
+
+template <class E, int VPT>
+struct GammaSmem {
+    static constexpr int NP = E::EPV / 2;
+    uint32_t base;
+    int tid, T, nv;
+    __device__ __forceinline__ void init(uint32_t tab, const uint4* gp, int t, int TT, int n, float2 off)
+    {
+        base = tab;
+        tid = t;
+        T = TT;
+        nv = n;
+        for (int v = t; v < n; v += TT) {
+            float2 f[NP];
+            E::pairs(__ldg(gp + v), f);
+#pragma unroll
+            for (int j = 0; j < NP; ++j) f[j] = add2(f[j], off);
+            st_shared_v4(base + v * 16u, make_uint4(__float_as_uint(f[0].x), __float_as_uint(f[0].y),
+                                                    __float_as_uint(f[1].x), __float_as_uint(f[1].y)));
+            st_shared_v4(base + (n + v) * 16u, make_uint4(__float_as_uint(f[2].x), __float_as_uint(f[2].y),
+                                                          __float_as_uint(f[3].x), __float_as_uint(f[3].y)));
+        }
+    }
+    __device__ __forceinline__ void load(const uint4*, int, int, int, float2, int = 1) {}
+    __device__ __forceinline__ void get(int k, float2 (&out)[NP]) const
+    {
+        const int v = tid + k * T;
+        uint4 a = make_uint4(0, 0, 0, 0), b = a;
+        if (v < nv) {
+            a = ld_shared_v4(base + v * 16u);
+            b = ld_shared_v4(base + (nv + v) * 16u);
+        }
+        out[0] = make_float2(__uint_as_float(a.x), __uint_as_float(a.y));
+        out[1] = make_float2(__uint_as_float(a.z), __uint_as_float(a.w));
+        out[2] = make_float2(__uint_as_float(b.x), __uint_as_float(b.y));
+        out[3] = make_float2(__uint_as_float(b.z), __uint_as_float(b.w));
+    }
+};
+
 // Shared memory after the stage rings: [2][32] float2 sum-of-squares partials, [2][32] row
 // maxima, [128] NVFP4 element factors gs / dec(s) indexed by the E4M3 block-scale code (the
 // row-per-warp schedule reduces in registers and keeps only the factor table), then per ring
 // [stages] mbarriers and [stages] row numbers of the slots, then (SCHED_CLUSTER) the cluster
 // exchange slots: [3] float4 {sum hi, sum lo, max, stop}, used in turn, and [2] float4
-// {amax, -, -, -}.
+// {amax, -, -, -}, or (FP8 with a weight offset on the CTA-per-row ring) the GammaSmem table of w.
 constexpr int kRedFloats = 2 * 32 * 2 + 2 * 32 + 128;
 constexpr int kRedFloatsWarp = 128;
 constexpr int kClusterXchBytes = 5 * 16;
@@ -729,10 +820,27 @@ constexpr int kClusterXchBytes = 5 * 16;
 // The kernel
 // ------------------------------------------------------------------------------------------
 
+// The FP8 kernels with a weight offset and 16-bit input hold y in registers between the two
+// row reductions (four vectors per thread) and take w from a shared-memory table (GammaSmem, on
+// the CTA-per-row ring) or re-read gamma from L1 (GammaL1, the other schedules).
+template <int DT, int MODE, int VPT, int SCHED, bool W16>
+__host__ __device__ constexpr bool fp8_offset16()
+{
+    return MODE == MODE_FP8 && !W16 && DT != DT_F32 && VPT == 4 && SCHED != SCHED_CLUSTER;
+}
+
+// Registers per thread: those kernels are capped at 80 so that three CTAs of 256 threads fit an
+// SM (measured on GB300: the cap costs no spills there); the rest take what 512 threads allow.
+template <int DT, int MODE, int VPT, int SCHED, bool W16>
+__host__ __device__ constexpr int reg_cap()
+{
+    return fp8_offset16<DT, MODE, VPT, SCHED, W16>() ? 80 : 128;
+}
+
 // W16: 16-bit input with weight_offset 0, so w = gamma is a 16-bit value and s * w, s^2 are
 // exact products formed straight from packed halves by mixed-precision FMA (no unpacking).
 template <int DT, bool RES, int MODE, int VPT, int SCHED, bool W16>
-__global__ void __launch_bounds__(512, 1)
+__global__ void __launch_bounds__(512, 1) __maxnreg__((reg_cap<DT, MODE, VPT, SCHED, W16>()))
 rmsq_row_kernel(const Params p)
 {
     using E = Elem<DT>;
@@ -790,6 +898,7 @@ rmsq_row_kernel(const Params p)
     float2* red_ss_all = reinterpret_cast<float2*>(red);                    // [2][32]
     float* red_max_all = red + 128;                                         // [2][32]
     float* nv_factor = WARP_ROWS ? red : red + 192;                         // [128]
+
     uint64_t* bars_all =
         reinterpret_cast<uint64_t*>(red + (WARP_ROWS ? kRedFloatsWarp : kRedFloats));  // [nrings][S]
     long long* rows_all = reinterpret_cast<long long*>(bars_all + S * nrings);        // [nrings][S]
@@ -906,7 +1015,14 @@ rmsq_row_kernel(const Params p)
     if constexpr (RING || MODE == MODE_NVFP4) __syncthreads();
 
     const float2 offset2 = splat(p.offset);
-    GammaRegs<E, VPT, !W16 && VPT <= 4> G;
+    constexpr bool GAMMA_L1 = fp8_offset16<DT, MODE, VPT, SCHED, W16>();
+    constexpr bool GAMMA_SMEM = GAMMA_L1 && SCHED == SCHED_PIPE;
+    std::conditional_t<GAMMA_SMEM, GammaSmem<E, VPT>,
+                       std::conditional_t<GAMMA_L1, GammaL1<E, VPT>, GammaRegs<E, VPT, !W16 && VPT <= 4>>> G;
+    if constexpr (GAMMA_SMEM) {
+        G.init(smem_u32(xch), static_cast<const uint4*>(p.gamma) + voff, rt, RT, nv, splat(p.offset));
+        __syncthreads();
+    }
     G.load(static_cast<const uint4*>(p.gamma) + voff, rt, RT, nv, offset2, NV_BLOCKED ? GROUP : 1);
     constexpr bool sw_exact = W16;                            // s * gamma exact in fp32
     const float Hf = static_cast<float>(p.hidden);
@@ -1011,13 +1127,24 @@ rmsq_row_kernel(const Params p)
                         acc_hi = E::sq_acc(sv[2], acc_hi);
                         acc_lo = E::sq_acc(sv[3], acc_lo);
                     }
+                } else if constexpr (EXACT && DT != DT_F32) {
+                    // exact squares straight from the packed halves (mixed-precision FMA)
+                    const uint32_t sv[4] = {s[k].x, s[k].y, s[k].z, s[k].w};
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const float2 sq = E::mul_halves(sv[j], sv[j]);
+                        float2 t, e;
+                        two_sum2(acc_hi, sq, t, e);
+                        acc_hi = t;
+                        acc_lo = add2(acc_lo, e);
+                    }
                 } else {
                     float2 f[NP];
                     E::pairs(s[k], f);
 #pragma unroll
                     for (int j = 0; j < NP; ++j) {
                         if constexpr (EXACT) {
-                            const float2 sq = mul2(f[j], f[j]);          // exact for 16-bit inputs
+                            const float2 sq = mul2(f[j], f[j]);          // fp32: hi part of f^2
                             float2 t, e;
                             two_sum2(acc_hi, sq, t, e);
                             acc_hi = t;
@@ -1036,19 +1163,38 @@ rmsq_row_kernel(const Params p)
         float* red_max = red_max_all + rbuf * 32;
         rbuf ^= 1;
         if constexpr (ONE_BAR) {
-            pmax = warp_max(pmax);
+            pmax = warp_max_abs(pmax);
             if (!WARP_ROWS && lane == 0) red_max[warp] = pmax;
         }
         FF ss;
         if constexpr (EXACT) {
             ss = ff_add(FF{acc_hi.x, acc_lo.x}, FF{acc_hi.y, acc_lo.y});
 #pragma unroll
-            for (int o = 16; o > 0; o >>= 1) ss = ff_add(ss, shfl_xor_ff(ss, o));
+            for (int o = 16; o > 0; o >>= 1) ss = ff_add_pos(ss, shfl_xor_ff(ss, o));
         } else {
             ss = FF{warp_sum(__fadd_rn(__fadd_rn(acc_hi.x, acc_hi.y), __fadd_rn(acc_lo.x, acc_lo.y))), 0.0f};
         }
         if (!WARP_ROWS && lane == 0) red_ss[warp] = make_float2(ss.hi, ss.lo);
         bool stop;
+        // the row's FP8 scale from its amax (rounded to the scale output type, whose value the
+        // codes are formed against), stored by `writer`
+        auto fp8_scale = [&](float amax, bool writer) -> float {
+            float sc = __fdiv_rn(fminf(amax, p.scale_ub), 448.0f);
+            if (p.scale_dtype == DT_BF16) {
+                uint16_t h;
+                asm("cvt.rn.bf16.f32 %0, %1;" : "=h"(h) : "f"(sc));
+                sc = __uint_as_float(static_cast<uint32_t>(h) << 16);
+                if (writer) static_cast<uint16_t*>(p.scale_out)[row] = h;
+            } else if (p.scale_dtype == DT_FP16) {
+                uint16_t h;
+                asm("cvt.rn.f16.f32 %0, %1;" : "=h"(h) : "f"(sc));
+                asm("cvt.f32.f16 %0, %1;" : "=f"(sc) : "h"(h));
+                if (writer) static_cast<uint16_t*>(p.scale_out)[row] = h;
+            } else {
+                if (writer) static_cast<float*>(p.scale_out)[row] = sc;
+            }
+            return sc;
+        };
         if constexpr (WARP_ROWS) stop = __any_sync(0xFFFFFFFFu, timed_out);
         else stop = __syncthreads_or(timed_out);
         // the row's (or, for SCHED_CLUSTER, this CTA's slice's) sum of squares and ONE_BAR max,
@@ -1061,7 +1207,7 @@ rmsq_row_kernel(const Params p)
                 FF t{part.x, part.y};
 #pragma unroll
                 for (int o = 8; o > 0; o >>= 1)
-                    if (o < red_lanes) t = ff_add(t, shfl_xor_ff(t, o));
+                    if (o < red_lanes) t = ff_add_pos(t, shfl_xor_ff(t, o));
                 tot.hi = __shfl_sync(0xFFFFFFFFu, t.hi, 0);
                 tot.lo = __shfl_sync(0xFFFFFFFFu, t.lo, 0);
                 if constexpr (ONE_BAR) {
@@ -1251,7 +1397,7 @@ rmsq_row_kernel(const Params p)
                     }
                     amax = fmaxf(amax, absmax_pairs(yy));
                 }
-                amax = warp_max(amax);
+                amax = warp_max_abs(amax);
                 if constexpr (!WARP_ROWS) {
                     if (lane == 0) red_max[warp] = amax;
                     __syncthreads();
@@ -1271,22 +1417,11 @@ rmsq_row_kernel(const Params p)
                     amax = mx;
                 }
             }
-            float scale = __fdiv_rn(fminf(amax, p.scale_ub), 448.0f);
-            if (p.scale_dtype == DT_BF16) {
-                uint16_t h;
-                asm("cvt.rn.bf16.f32 %0, %1;" : "=h"(h) : "f"(scale));
-                scale = __uint_as_float(static_cast<uint32_t>(h) << 16);
-                if (rt == 0 && crank == 0) static_cast<uint16_t*>(p.scale_out)[row] = h;
-            } else if (p.scale_dtype == DT_FP16) {
-                uint16_t h;
-                asm("cvt.rn.f16.f32 %0, %1;" : "=h"(h) : "f"(scale));
-                asm("cvt.f32.f16 %0, %1;" : "=f"(scale) : "h"(h));
-                if (rt == 0 && crank == 0) static_cast<uint16_t*>(p.scale_out)[row] = h;
-            } else {
-                if (rt == 0 && crank == 0) static_cast<float*>(p.scale_out)[row] = scale;
-            }
-            const bool zero_row = !(scale > 0.0f);
-            const float2 inv2 = splat(zero_row ? 0.0f : __frcp_rn(scale));
+            const float scale = fp8_scale(amax, rt == 0 && crank == 0);
+            const float inv = scale > 0.0f ? __frcp_rn(scale) : 0.0f;
+            // a zero scale (all-zero row) gives inv = 0, so every quotient below is a zero and
+            // every code 0x00 (or 0x80 for a negative zero y: the same value)
+            const float2 inv2 = splat(inv);
             const float2 nd2 = splat(-scale);
             unsigned char* outp = static_cast<unsigned char*>(p.out) + row * p.hidden +
                                   static_cast<long long>(voff) * EPV;
@@ -1310,7 +1445,7 @@ rmsq_row_kernel(const Params p)
             auto store_codes = [&](int v, const float2 (&q)[NP]) {
                 uint32_t c[NP];
 #pragma unroll
-                for (int j = 0; j < NP; ++j) c[j] = zero_row ? 0u : cvt_e4m3x2(q[j].x, q[j].y);
+                for (int j = 0; j < NP; ++j) c[j] = cvt_e4m3x2(q[j].x, q[j].y);
                 if constexpr (EPV == 8) {
                     st_v2(outp + v * 8, c[0] | (c[1] << 16), c[2] | (c[3] << 16));
                 } else {
@@ -1536,7 +1671,7 @@ rmsq_row_kernel(const Params p)
     if (aborted) return;
     if constexpr (MODE == MODE_AMAX) {
         // non-negative floats order like their bit patterns, so an unsigned max is a float max
-        run_max = warp_max(run_max);
+        run_max = warp_max_abs(run_max);
         if (lane == 0 && run_max > 0.0f)
             atomicMax(static_cast<unsigned int*>(p.scale_out), __float_as_uint(run_max));
     }
