@@ -725,6 +725,24 @@ def report_workloads():
     return names
 
 
+class L2Flush:
+    """Evicts L2 between timed repetitions with a 256 MiB pass over a device buffer, about twice
+    the 129 MB L2. `write` fills it (the timing rules' flush: the timed launch then also pays
+    for writing those dirty lines back); `read` reads it, which leaves only clean lines, for
+    kernels that read far more than they write (the global-scale pre-pass writes 4 bytes)."""
+
+    def __init__(self, kind="write"):
+        self.kind = kind
+        self.buf = (torch.empty(256 << 20, dtype=torch.uint8, device="cuda") if kind == "write"
+                    else torch.ones(64 << 20, dtype=torch.float32, device="cuda"))
+
+    def __call__(self):
+        if self.kind == "write":
+            self.buf.fill_(1)
+        else:
+            self.buf.amax()
+
+
 def run_report(args):
     from rmsnorm_precision_activation_gb300 import build as B
     B.build()
@@ -732,7 +750,7 @@ def run_report(args):
     torch.cuda.set_device(0)
     peak, _ = measured_peak()
     cpu = host_cpu()
-    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    flush = L2Flush(args.flush)
     only = set(args.only.split(",")) if args.only else None
     for name, rows, hidden in report_workloads():
         if only and name not in only and "%s:%s:%s" % (name, rows, hidden) not in only:
@@ -753,7 +771,7 @@ def run_report(args):
             fn()
         times = []
         for _ in range(args.report_reps):
-            flush.fill_(1)                      # evict L2 between repetitions
+            flush()                             # evict L2 between repetitions
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record()
             fn()
@@ -767,7 +785,7 @@ def run_report(args):
                 "algorithmic_bytes": w.algorithmic_bytes(), "gbs": round(gbs, 1),
                 "rows_per_s": round(w.rows / (us * 1e-6)),
                 "frac_of_measured": round(gbs / peak, 4),
-                "pct_of_8tbs": round(100 * gbs / NOMINAL_HBM_GBS, 2)}
+                "pct_of_8tbs": round(100 * gbs / NOMINAL_HBM_GBS, 2), "l2_flush": args.flush}
         del outs, d
         if args.oracle_seconds > 0:
             # the oracle beside the GPU figure: a reported baseline, not the target
@@ -836,7 +854,7 @@ def _time_launch(fn, flush, reps):
         fn()
     times = []
     for _ in range(reps):
-        flush.fill_(1)                               # evict L2 between repetitions
+        flush()                                      # evict L2 between repetitions
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record()
         fn()
@@ -854,7 +872,7 @@ def run_report_next(args):
     import rmsnorm_precision_activation_gb300 as rq
     torch.cuda.set_device(0)
     peak, _ = measured_peak()
-    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    flush = L2Flush(args.flush)
 
     def launcher(w, d, opts):
         x, r, g = d["input"], d["residual"], d["gamma"]
@@ -888,7 +906,7 @@ def run_report_next(args):
                 "options": {k: (str(v).replace("torch.", "") if isinstance(v, torch.dtype) else v)
                             for k, v in opts.items()},
                 "us": round(us, 2), "algorithmic_bytes": nb, "gbs": round(nb / (us * 1e-6) / 1e9, 1),
-                "frac_of_measured": round(nb / (us * 1e-6) / 1e9 / peak, 4)}
+                "frac_of_measured": round(nb / (us * 1e-6) / 1e9 / peak, 4), "l2_flush": args.flush}
         if case in ("fp32_input", "fp16_input"):
             db = W.generate(w, seed=0, device="cuda")
             line["base_us"] = round(_time_launch(launcher(w, db, {}), flush, args.report_reps), 2)
@@ -974,6 +992,9 @@ def main():
     ap.add_argument("--report-next", action="store_true",
                     help="time the widened rows (swizzled scales, global-scale pre-pass, other "
                          "dtypes, cluster rows), one JSON line each")
+    ap.add_argument("--flush", choices=["write", "read"], default="write",
+                    help="--report / --report-next: evict L2 between repetitions by writing a "
+                         "256 MiB buffer (default) or by reading one (clean lines only)")
     ap.add_argument("--only", default="", help="--report: comma-separated workload names "
                     "(or name:rows:hidden for one MXFP4 sweep point); --report-next: case names "
                     "(or case:mode:rows:hidden)")

@@ -173,15 +173,16 @@ cudaError_t run_kernel(const void* fn, const Plan& pl, const Params& p, cudaStre
     const long long procs = grid * rows_per_cta;
     q.rowctr = nullptr;
     q.rows_static = p.rows;
-    if (g_dynamic_rows.load() && pl.sched == SCHED_PIPE && di.counters != nullptr && p.rows >= 2 * procs &&
+    // this launch's scratch slot of the pool: [0] the row counter, [1..2] the pre-pass's max
+    // and done count
+    unsigned int* slot = nullptr;
+    if (di.counters != nullptr)
+        slot = di.counters + (g_counter_seq.fetch_add(1) % kCounterSlots) * 8;
+    q.amax_slot = slot != nullptr ? slot + 1 : nullptr;
+    if (g_dynamic_rows.load() && pl.sched == SCHED_PIPE && slot != nullptr && p.rows >= 2 * procs &&
         p.rows < (1LL << 31)) {
         // a counter the caller set up (zeroed, on this stream) is used as it is
-        if (p.rowctr != nullptr) {
-            q.rowctr = p.rowctr;
-        } else {
-            const unsigned long long slot = g_counter_seq.fetch_add(1) % kCounterSlots;
-            q.rowctr = di.counters + slot * 8;
-        }
+        q.rowctr = p.rowctr != nullptr ? p.rowctr : slot;
         q.rows_static = p.rows / procs * 3 / 4 * procs;
     }
     void* args[] = {&q};
@@ -224,8 +225,9 @@ static int elems_per_vec(int dt) { return dt == DT_F32 ? 4 : 8; }
 //    - FP4 with a residual: 2 vectors per thread up to 1024 vectors per row, then as many as
 //      make 512 threads (NVFP4 rows of up to 512 vectors: 4);
 //    - FP8 rows of up to 256 vectors: 4 vectors per thread and about 12 warps per SM.
-//  - A two-row ring per CTA; three for FP4 rows with a residual of 256-511 vectors, or of
-//    2048 vectors and more (one CTA per SM then).
+//  - A two-row ring per CTA; three for FP4 rows with a residual of 2048 vectors and more (one
+//    CTA per SM then); the FP8 kernel with a weight offset and 16-bit input: one or two slots
+//    beside its w table (below).
 //  - CTAs per SM (shared memory permitting):
 //    - FP4 with a residual: 8;
 //    - the W16 FP8 kernel: 4; the other FP8 kernels: 6;
@@ -273,7 +275,7 @@ static bool make_plan(int mode, int dt, bool res, bool w16, int hidden, const De
     // (three CTAs per SM, so one CTA's row-end barrier and exchange overlap the others' work;
     // measured on GB300: 4.5-5.1 TB/s against 3.7-4.5 TB/s with one CTA per SM at 32768), else
     // the smallest whose ring fits; slices hold whole FP4 scale blocks; 4 or 8 vectors per
-    // thread, at most 256 threads.
+    // thread, at most 256 threads (FP8: 512).
     const int red_bytes = kRedFloats * 4;
     const bool pipe_fits = 2 * stage + red_bytes + 2 * 16 <= di.smem_optin;
     if (forced == SCHED_CLUSTER || (!pipe_fits && forced != SCHED_REG)) {
@@ -304,10 +306,13 @@ static bool make_plan(int mode, int dt, bool res, bool w16, int hidden, const De
         if (best != 0) {
             const int nvc = nv / best;
             const long long cstage = static_cast<long long>(nvc) * 16 * (res ? 2 : 1);
+            // (FP8: up to 512 threads with 4 vectors each; measured on GB300 at 2048 x 131072,
+            // 484 us against 529 us with 8 vectors and 256 threads)
             int cv = g_tune_vpt.load();
             if (cv < 4 || (nvc + cv - 1) / cv > 512) {        // instantiated for 4 and 8
                 cv = 4;
-                while (cv < 8 && nvc > 256 * cv) cv *= 2;
+                const int per = mode == MODE_FP8 ? 512 : 256;
+                while (cv < 8 && nvc > per * cv) cv *= 2;
             }
             // ring slots, reduction area, per slot an mbarrier and a row number, exchange slots.
             // Kernels with one exchange per row (all but FP8 with an offset or fp32 input) hold
@@ -389,7 +394,7 @@ static bool make_plan(int mode, int dt, bool res, bool w16, int hidden, const De
     } else if (pl.sched == SCHED_PIPE) {
         int stages = g_tune_stages.load();
         if (stages == 0)
-            stages = (mode != MODE_FP8 && res && ((nv >= 256 && nv < 512) || nv >= 2048)) ? 3 : 2;
+            stages = (mode != MODE_FP8 && res && nv >= 2048) ? 3 : 2;
         // ring slots, reduction area, then per slot an mbarrier and the slot's row number
         while (stages > 2 && stages * stage + red_bytes + stages * 16 > di.smem_optin) --stages;
         pl.stages = stages;
@@ -503,12 +508,8 @@ __global__ void debug_convert_kernel(int fmt, const float* __restrict__ in,
     }
 }
 
-// gs = 448 * 6 / amax, where *gs holds amax's bits on entry; an all-zero tensor gives gs = 1.
-__global__ void finalize_global_scale_kernel(float* gs)
-{
-    const float amax = __uint_as_float(*reinterpret_cast<unsigned int*>(gs));
-    *gs = amax > 0.0f ? __fdiv_rn(448.0f * 6.0f, amax) : 1.0f;
-}
+// The global scale of a tensor with no rows (max |y| = 0): 1.
+__global__ void global_scale_of_empty_kernel(float* gs) { *gs = 1.0f; }
 
 }  // namespace rmsq
 
@@ -679,18 +680,15 @@ extern "C" rmsq_status rmsnorm_nvfp4_global_scale(const void* input, const void*
     const DeviceInfo* di = device_info();
     if (!di) return RMSQ_ERR_DEVICE;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (cudaMemsetAsync(gs_out, 0, sizeof(float), s) != cudaSuccess) {
-        cudaGetLastError();
-        return RMSQ_ERR_LAUNCH;
-    }
     if (rows > 0) {
+        // one launch: its last CTA writes gs (the kernel's epilogue)
         Params p = base_params(input, residual, nullptr, gamma, rows, hidden, dtype, epsilon,
                                weight_offset, *di);
         p.scale_out = gs_out;
-        rmsq_status ls = launch(MODE_AMAX, p, residual != nullptr, dtype, *di, s);
-        if (ls != RMSQ_OK) return ls;
+        return launch(MODE_AMAX, p, residual != nullptr, dtype, *di, s);
     }
-    finalize_global_scale_kernel<<<1, 1, 0, s>>>(gs_out);
+    // no rows: an all-zero tensor's gs, 1
+    global_scale_of_empty_kernel<<<1, 1, 0, s>>>(gs_out);
     if (cudaGetLastError() != cudaSuccess) return RMSQ_ERR_LAUNCH;
     g_launches.fetch_add(1, std::memory_order_relaxed);
     return RMSQ_OK;

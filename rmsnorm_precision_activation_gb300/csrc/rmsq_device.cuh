@@ -71,6 +71,9 @@ struct Params {
     // which starts at 0 and is left at 0. rowctr may be null, with rows_static = rows.
     unsigned int* rowctr;
     long long rows_static;
+    // MODE_AMAX: two words of the launch's scratch slot, both 0 at launch and left at 0: [0] the
+    // running max |y| (bits), [1] the count of CTAs done. The last CTA turns the max into gs.
+    unsigned int* amax_slot;
 };
 
 // ------------------------------------------------------------------------------------------
@@ -864,7 +867,13 @@ rmsq_row_kernel(const Params p)
     // registers across the CTA barrier (the slot is refilled after an end-of-row barrier). That
     // pays except for the FP8 kernels with an offset or fp32 input (instruction-bound: they keep s
     // and y in registers and refill the slot right after the sum-of-squares barrier).
-    constexpr bool SMEM_S = RING && (MODE != MODE_FP8 || W16);
+    //
+    // The global-scale pre-pass needs no second pass over the row: each thread keeps
+    // max |s w| of its elements from pass 1, and max |y| = RN(rstd * that) per thread (rstd > 0
+    // and rounding is monotonic), so its slot is refilled right after the sum-of-squares
+    // barrier. Its cluster schedule keeps the slot (PIPE_X finishes each row one row later).
+    constexpr bool AMAX_P1 = MODE == MODE_AMAX && SCHED != SCHED_CLUSTER;
+    constexpr bool SMEM_S = RING && (MODE != MODE_FP8 || W16) && !AMAX_P1;
     // NVFP4 with a ring: pass 2 is blocked, each thread owns whole 16-element scale blocks
     // (GROUP consecutive vectors, re-read from the slot), so the block scale, its table lookup
     // and its store happen once per block and the codes leave in one 8-byte store.
@@ -1081,7 +1090,7 @@ rmsq_row_kernel(const Params p)
         // ---- load the row, add the residual, write residual_output, sum of squares ----------
         uint4 s[VPT];
         float2 acc_hi = make_float2(0.0f, 0.0f), acc_lo = make_float2(0.0f, 0.0f);
-        float pmax = 0.0f;      // ONE_BAR: max |s w| over this thread's elements
+        float pmax = 0.0f;      // ONE_BAR and the pre-pass: max |s w| over this thread's elements
 #pragma unroll
         for (int k = 0; k < VPT; ++k) {
             const int v = rt + k * RT;
@@ -1126,6 +1135,13 @@ rmsq_row_kernel(const Params p)
                         acc_lo = E::sq_acc(sv[1], acc_lo);
                         acc_hi = E::sq_acc(sv[2], acc_hi);
                         acc_lo = E::sq_acc(sv[3], acc_lo);
+                        if constexpr (AMAX_P1) {
+                            const uint32_t gv[4] = {G.g[k].x, G.g[k].y, G.g[k].z, G.g[k].w};
+                            float2 pw[NP];
+#pragma unroll
+                            for (int j = 0; j < NP; ++j) pw[j] = E::mul_halves(sv[j], gv[j]);
+                            pmax = fmaxf(pmax, absmax_pairs(pw));
+                        }
                     }
                 } else if constexpr (EXACT && DT != DT_F32) {
                     // exact squares straight from the packed halves (mixed-precision FMA)
@@ -1154,6 +1170,13 @@ rmsq_row_kernel(const Params p)
                         } else {
                             acc_hi = fma2(f[j], f[j], acc_hi);
                         }
+                    }
+                    if constexpr (AMAX_P1) {
+                        float2 w[NP];
+                        G.get(k, w);
+#pragma unroll
+                        for (int j = 0; j < NP; ++j) f[j] = mul2(f[j], w[j]);
+                        pmax = fmaxf(pmax, absmax_pairs(f));
                     }
                 }
             }
@@ -1360,12 +1383,14 @@ rmsq_row_kernel(const Params p)
 
         if constexpr (MODE == MODE_AMAX) {
             // max |y| = rstd * max |s w| (rstd > 0, rounding is monotonic)
-            float mp = 0.0f;
+            float mp = pmax;
+            if constexpr (!AMAX_P1) {
 #pragma unroll
-            for (int k = 0; k < VPT; ++k) {
-                float2 sw[NP];
-                sw_pairs(k, sw);
-                mp = fmaxf(mp, absmax_pairs(sw));
+                for (int k = 0; k < VPT; ++k) {
+                    float2 sw[NP];
+                    sw_pairs(k, sw);
+                    mp = fmaxf(mp, absmax_pairs(sw));
+                }
             }
             if (mp > 0.0f) run_max = fmaxf(run_max, __fmul_rn(mp, rstd));
         } else if constexpr (MODE == MODE_FP8) {
@@ -1668,13 +1693,32 @@ rmsq_row_kernel(const Params p)
         }
     }
     if constexpr (CLUSTER) cluster_sync();   // no CTA leaves while others may read its slots
-    if (aborted) return;
     if constexpr (MODE == MODE_AMAX) {
-        // non-negative floats order like their bit patterns, so an unsigned max is a float max
-        run_max = warp_max_abs(run_max);
-        if (lane == 0 && run_max > 0.0f)
-            atomicMax(static_cast<unsigned int*>(p.scale_out), __float_as_uint(run_max));
+        // The CTA's max |y| joins the launch's running max (non-negative floats order like their
+        // bit patterns, so an unsigned max is a float max); then the CTA counts itself done. The
+        // last CTA to do so reads the max, writes gs = 448 * 6 / max (1 for an all-zero tensor)
+        // and leaves both words at 0 for the slot's next launch. A CTA stopped by a timed-out
+        // wait still counts itself (the error word already reports the launch).
+        const float wm = warp_max_abs(run_max);
+        __syncthreads();                       // every warp is out of the row loop: `red` is free
+        if (lane == 0) red[warp] = wm;
+        __syncthreads();
+        if (tid == 0) {
+            float cm = 0.0f;
+            for (int w = 0; w < nwarps; ++w) cm = fmaxf(cm, red[w]);
+            if (!aborted && cm > 0.0f) atomicMax(p.amax_slot, __float_as_uint(cm));
+            __threadfence();
+            const unsigned int done = atomicAdd(p.amax_slot + 1, 1u);
+            if (done == gridDim.x - 1) {
+                __threadfence();
+                const float amax = __uint_as_float(atomicExch(p.amax_slot, 0u));
+                atomicExch(p.amax_slot + 1, 0u);
+                *static_cast<float*>(p.scale_out) = amax > 0.0f ? __fdiv_rn(448.0f * 6.0f, amax) : 1.0f;
+            }
+        }
+        return;
     }
+    if (aborted) return;
 }
 
 }  // namespace rmsq

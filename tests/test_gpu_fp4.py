@@ -83,3 +83,28 @@ def test_swizzled_padding_untouched():
     used = {oracle.scale_offset(r, s, H // 16, True) for r in range(rows) for s in range(H // 16)}
     pad = np.array(sorted(set(range(n)) - used))
     assert len(pad) > 0 and np.all(flat[pad] == 0xA5)
+
+
+def test_global_scale_prepass_reuses_its_scratch_slots():
+    """The pre-pass is one launch whose last CTA turns the launch's running max into gs and
+    leaves its two scratch words at 0. Launches take their slot from a pool of 4096 in turn, so
+    4200 launches (alternating two inputs whose global scales differ, with and without a
+    residual, and one with no rows) reuse slots; every gs must still be that input's."""
+    wa = W.Workload("custom", "nvfp4", 48, 2048, "bf16", True)
+    wb = W.Workload("custom", "nvfp4", 300, 1024, "bf16", False)
+    da, db = inputs(wa, seed=61), inputs(wb, seed=62)
+    db["input"] = db["input"] * 3
+    ga, gb = float(oracle_global_scale(wa, da)), float(oracle_global_scale(wb, db))
+    n = 4200
+    out = torch.empty(n + 1, dtype=torch.float32, device="cuda")
+    for i in range(n):
+        w, d = (wa, da) if i % 2 == 0 else (wb, db)
+        rq().rmsnorm_nvfp4_global_scale(d["input"], d["gamma"], residual=d["residual"],
+                                        epsilon=w.eps, out=out[i:i + 1])
+    empty = torch.empty(0, 2048, dtype=torch.bfloat16, device="cuda")
+    rq().rmsnorm_nvfp4_global_scale(empty, da["gamma"], epsilon=wa.eps, out=out[n:n + 1])
+    got = out.cpu().numpy()
+    assert np.all(np.abs(got[0:n:2] - ga) <= 2e-6 * ga)
+    assert np.all(np.abs(got[1:n:2] - gb) <= 2e-6 * gb)
+    assert got[n] == 1.0
+    assert rq().rmsq_device_status() == 0
