@@ -230,7 +230,8 @@ static int elems_per_vec(int dt) { return dt == DT_F32 ? 4 : 8; }
 //    beside its w table (below).
 //  - CTAs per SM (shared memory permitting):
 //    - FP4 with a residual: 8;
-//    - the W16 FP8 kernel: 4; the other FP8 kernels: 6;
+//    - the W16 FP8 kernel: 8 (measured on GB300 at 8192 x 4096: 37.5 us against 41.6 us with
+//      4); the other FP8 kernels: 6;
 //    - FP4 without a residual: 8.
 static bool make_plan(int mode, int dt, bool res, bool w16, int hidden, const DeviceInfo& di,
                       Plan& pl)
@@ -361,7 +362,7 @@ static bool make_plan(int mode, int dt, bool res, bool w16, int hidden, const De
     pl.sched = (forced == SCHED_REG || !pipe_fits) ? SCHED_REG : SCHED_PIPE;
     pl.ctas_per_sm = g_tune_ctas.load();
     if (pl.ctas_per_sm == 0) {
-        if (mode == MODE_FP8) pl.ctas_per_sm = nv <= 256 ? 384 / threads : (w16 ? 4 : 6);
+        if (mode == MODE_FP8) pl.ctas_per_sm = nv <= 256 ? 384 / threads : (w16 ? 8 : 6);
         else if (!res) pl.ctas_per_sm = 8;
         else pl.ctas_per_sm = 8;
     }

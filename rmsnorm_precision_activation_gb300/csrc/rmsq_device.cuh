@@ -737,6 +737,8 @@ struct GammaRegs<E, VPT, false> {
 #pragma unroll
         for (int j = 0; j < NP; ++j) out[j] = add2(out[j], off);
     }
+    // the 16-byte gamma vector k, as stored
+    __device__ __forceinline__ uint4 packed(int k) const { return g[k]; }
 };
 
 // w for the FP8 kernels with a weight offset and 16-bit input: no registers held across the
@@ -1123,7 +1125,8 @@ rmsq_row_kernel(const Params p)
                             acc_lo = add2(acc_lo, e);
                         }
                         if constexpr (ONE_BAR) {
-                            const uint32_t gv[4] = {G.g[k].x, G.g[k].y, G.g[k].z, G.g[k].w};
+                            const uint4 gk = G.packed(k);
+                            const uint32_t gv[4] = {gk.x, gk.y, gk.z, gk.w};
                             float2 pw[NP];
 #pragma unroll
                             for (int j = 0; j < NP; ++j) pw[j] = E::mul_halves(sv[j], gv[j]);
@@ -1136,7 +1139,8 @@ rmsq_row_kernel(const Params p)
                         acc_hi = E::sq_acc(sv[2], acc_hi);
                         acc_lo = E::sq_acc(sv[3], acc_lo);
                         if constexpr (AMAX_P1) {
-                            const uint32_t gv[4] = {G.g[k].x, G.g[k].y, G.g[k].z, G.g[k].w};
+                            const uint4 gk = G.packed(k);
+                            const uint32_t gv[4] = {gk.x, gk.y, gk.z, gk.w};
                             float2 pw[NP];
 #pragma unroll
                             for (int j = 0; j < NP; ++j) pw[j] = E::mul_halves(sv[j], gv[j]);
@@ -1369,7 +1373,8 @@ rmsq_row_kernel(const Params p)
             const uint4 sk = get_s(k);
             if constexpr (W16) {
                 const uint32_t sv[4] = {sk.x, sk.y, sk.z, sk.w};
-                const uint32_t gv[4] = {G.g[k].x, G.g[k].y, G.g[k].z, G.g[k].w};
+                const uint4 gk = G.packed(k);
+                            const uint32_t gv[4] = {gk.x, gk.y, gk.z, gk.w};
 #pragma unroll
                 for (int j = 0; j < NP; ++j) out[j] = E::mul_halves(sv[j], gv[j]);
             } else {
@@ -1560,7 +1565,8 @@ rmsq_row_kernel(const Params p)
                     const int k = kb * GROUP + j;
                     if constexpr (W16) {
                         const uint32_t sv[4] = {sk.x, sk.y, sk.z, sk.w};
-                        const uint32_t gv[4] = {G.g[k].x, G.g[k].y, G.g[k].z, G.g[k].w};
+                        const uint4 gk = G.packed(k);
+                            const uint32_t gv[4] = {gk.x, gk.y, gk.z, gk.w};
 #pragma unroll
                         for (int i = 0; i < NP; ++i) sw[j][i] = E::mul_halves(sv[i], gv[i]);
                     } else {
