@@ -184,10 +184,17 @@ const char* rmsq_status_string(rmsq_status status);
 
 /* ---------------------------------------------------------------------------------------------
  * rmsq_device_status -- errors raised on the device since the last call, for the current device.
- * Every wait inside a kernel (on a bulk-copy barrier) is bounded in time; a wait that runs out
- * sets a flag, the kernel stops cleanly and its outputs are incomplete. This call synchronises
- * the device, returns RMSQ_ERR_TIMEOUT if a flag was set (RMSQ_OK otherwise) and clears it,
- * together with the row counters a stopped launch may have left behind.
+ * Every wait inside a kernel on a bulk-copy (mbarrier) phase is bounded in time; a wait that runs
+ * out sets a flag and the CTA stops, after waiting (for four times the bound) for the copies it
+ * has in flight. After RMSQ_ERR_TIMEOUT the outputs of the launches since the last call are not
+ * to be trusted. If one of those drain waits ran out as well (a second flag, reported the same
+ * way), a CTA may have exited with a copy into its shared memory still pending; treat the CUDA
+ * context as unreliable then. The cluster barrier of the cluster schedule is a hardware barrier
+ * that cannot be bounded: every CTA of a cluster makes the same barrier calls (a timed-out wait
+ * is shared through the cluster exchange and all CTAs stop together), so none is left waiting.
+ * This call synchronises the device, returns RMSQ_ERR_TIMEOUT if a flag was set (RMSQ_OK
+ * otherwise) and clears the flags, together with the scratch words (row counters, the
+ * global-scale pre-pass's maximum) a stopped launch may have left behind.
  * ------------------------------------------------------------------------------------------- */
 rmsq_status rmsq_device_status(void);
 

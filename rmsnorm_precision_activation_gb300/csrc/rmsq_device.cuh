@@ -43,7 +43,9 @@ enum { MODE_FP8 = 0, MODE_NVFP4 = 1, MODE_MXFP4 = 2, MODE_AMAX = 3 };
 enum { SCHED_PIPE = 1, SCHED_REG = 2, SCHED_WARP = 3, SCHED_CLUSTER = 4 };
 
 // Error flag bits set on the device.
-enum { ERRF_WAIT_TIMEOUT = 1u };
+// ERRF_DRAIN_TIMEOUT: after a timed-out wait, a CTA's wait for its own copies in flight also ran
+// out, so it may have exited while a copy into its shared memory was still outstanding.
+enum { ERRF_WAIT_TIMEOUT = 1u, ERRF_DRAIN_TIMEOUT = 2u };
 
 struct Params {
     const void* x;            // [rows x hidden]
@@ -1320,28 +1322,34 @@ rmsq_row_kernel(const Params p)
             if constexpr (RING) {
                 if (issuer) {
                     atomicOr(p.err, ERRF_WAIT_TIMEOUT);
-                    // Let the copies already issued into the ring's other slots land (bounded):
-                    // all after this row's slot, or (PIPE_X, where the ring has already moved
-                    // past the two rows held) all after the slot acquired last.
+                    // Before the CTA exits, let every copy it issued land: the slot whose wait ran
+                    // out and every later one (PIPE_X: from the slot acquired last, the ring
+                    // having moved past it). Each slot has one phase outstanding; a slot that is
+                    // already complete, or was armed empty, passes at once. These waits take four
+                    // times the bound; one that runs out as well is recorded, because the CTA
+                    // then exits with a copy into its shared memory possibly still pending.
                     int js = stage;
                     uint32_t jp = parity;
+                    int n = S;
                     if constexpr (PIPE_X) {
-                        for (int j = 0; j < S - 2; ++j) {
-                            mbar_wait_bounded(smem_u32(&bars[js]), jp, p.timeout_ns);
-                            if (++js == S) {
-                                js = 0;
-                                jp ^= 1u;
-                            }
+                        // back to the slot acquired last (cur_stage), then the S - 2 after it
+                        if (js == 0) {
+                            js = S - 1;
+                            jp ^= 1u;
+                        } else {
+                            --js;
                         }
-                    } else {
-                        for (int j = 1; j < S; ++j) {
-                            if (++js == S) {
-                                js = 0;
-                                jp ^= 1u;
-                            }
-                            mbar_wait_bounded(smem_u32(&bars[js]), jp, p.timeout_ns);
+                        n = S - 1;
+                    }
+                    bool drained = true;
+                    for (int j = 0; j < n; ++j) {
+                        drained = mbar_wait_bounded(smem_u32(&bars[js]), jp, 4 * p.timeout_ns) && drained;
+                        if (++js == S) {
+                            js = 0;
+                            jp ^= 1u;
                         }
                     }
+                    if (!drained) atomicOr(p.err, ERRF_DRAIN_TIMEOUT);
                 }
             }
             aborted = true;
