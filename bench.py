@@ -957,8 +957,9 @@ def ncu_table(args):
     per = 4 + args.report_reps
     mode_id = {"fp8": 0, "nvfp4": 1, "mxfp4": 2}
     print("| workload | rows x hidden | ncu duration (us) | DRAM read + write (MB) | algorithmic "
-          "MB | DRAM throughput (% of peak) | algorithmic GB/s at ncu duration |")
-    print("|---|---|---|---|---|---|---|")
+          "MB | DRAM throughput (% of peak) | min - max over launches (%) | algorithmic GB/s at "
+          "ncu duration |")
+    print("|---|---|---|---|---|---|---|---|")
     k = 0
     for name, rws, hid in report_workloads():
         if only and name not in only and "%s:%s:%s" % (name, rws, hid) not in only:
@@ -972,11 +973,12 @@ def ncu_table(args):
         med = lambda m: statistics.median(e[m] for e in timed)
         dur = med("gpu__time_duration.sum")
         traffic = med("dram__bytes_read.sum") + med("dram__bytes_write.sum")
-        pct = med("dram__throughput.avg.pct_of_peak_sustained_elapsed")
+        pcts = [e["dram__throughput.avg.pct_of_peak_sustained_elapsed"] for e in timed]
+        pct = statistics.median(pcts)
         algo = w.algorithmic_bytes()
-        print("| %s | %d x %d | %.1f | %.1f | %.1f | %.1f | %.0f |"
-              % (name, w.rows, w.hidden, dur * 1e6, traffic / 1e6, algo / 1e6, pct,
-                 algo / dur / 1e9))
+        print("| %s | %d x %d | %.1f | %.1f | %.1f | %.1f | %.1f - %.1f | %.0f |"
+              % (name, w.rows, w.hidden, dur * 1e6, traffic / 1e6, algo / 1e6, pct, min(pcts),
+                 max(pcts), algo / dur / 1e9))
     if k != len(seq):
         raise SystemExit("ncu CSV has %d launches left over" % (len(seq) - k))
 
