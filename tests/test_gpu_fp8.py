@@ -30,7 +30,8 @@ def test_fp8_full_size_sampled(name, sched):
     d = inputs(w, seed=0)
     with schedule(sched):
         rep, _ = check_fp8(w, d, idx=sample_rows(w.rows, 96, seed=1))
-    assert rep["bad"] == 0
+    # the FP8 kernels form the definition's fp32 values exactly: not even a tolerated code differs
+    assert rep["bad"] == 0 and rep["tolerated"] == 0
 
 
 def test_fp8_gemma_spike_clamps():
