@@ -71,3 +71,20 @@ def test_fp8_offset_and_tiny_ub():
     w = W.Workload("custom", "fp8", 200, 2048, "fp16", True, weight_offset=1.0, scale_ub=0.5)
     rep, ora = check_fp8(w, inputs(w, seed=4))
     assert rep["clamped_rows"] == 200
+
+
+@pytest.mark.parametrize("sched", [0, 1, 2, 3])
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16, torch.float32])
+@pytest.mark.parametrize("rows,hidden", [(37, 64), (301, 520), (1000, 2048), (700, 4104),
+                                         (455, 8192), (97, 12288), (60, 16384)])
+def test_fp8_weight_offset_shapes(rows, hidden, dtype, sched):
+    """The FP8 kernels with a weight offset: the CTA-per-row ring keeps w = gamma + offset in a
+    shared-memory table beside one or two ring slots (16-bit input), the other schedules and fp32
+    input take w from L1 or registers. Every plan must give the definition's codes exactly."""
+    if sched == 3 and hidden * torch.tensor([], dtype=dtype).element_size() > 4096:
+        pytest.skip("row per warp holds rows of up to 256 vectors")
+    w = W.Workload("custom", "fp8", rows, hidden, "fp16", True, weight_offset=0.75, scale_ub=6.0)
+    d = inputs(w, seed=rows * 7 + hidden, dtype=dtype)
+    with schedule(sched):
+        rep, _ = check_fp8(w, d)
+    assert rep["bad"] == 0 and rep["tolerated"] == 0
