@@ -272,14 +272,17 @@ static bool make_plan(int mode, int dt, bool res, bool w16, int hidden, const De
     }
 
     // A cluster of C CTAs per row: for rows whose two-slot ring does not fit one CTA's shared
-    // memory (or when forced). The smallest C of 2, 4, 8, 16 whose slice slot holds at most 32 KB
+    // memory or that need more than 512 threads (or when forced). The smallest C of 2, 4, 8, 16 whose slice slot holds at most 32 KB
     // (three CTAs per SM, so one CTA's row-end barrier and exchange overlap the others' work;
     // measured on GB300: 4.5-5.1 TB/s against 3.7-4.5 TB/s with one CTA per SM at 32768), else
     // the smallest whose ring fits; slices hold whole FP4 scale blocks; 4 or 8 vectors per
     // thread, at most 256 threads (FP8: 512).
     const int red_bytes = kRedFloats * 4;
     const bool pipe_fits = 2 * stage + red_bytes + 2 * 16 <= di.smem_optin;
-    if (forced == SCHED_CLUSTER || (!pipe_fits && forced != SCHED_REG)) {
+    // A CTA covers at most 512 threads x 8 vectors: wider rows take a cluster even when two of
+    // their ring slots would fit one CTA's shared memory (rows without a residual).
+    const bool one_cta = pipe_fits && nv <= 512 * 8;
+    if (forced == SCHED_CLUSTER || (!one_cta && forced != SCHED_REG)) {
         const int tune_c = g_tune_cluster.load();
         const int blk = mode == MODE_MXFP4 ? 32 : 16;
         int best = 0;
