@@ -147,7 +147,10 @@ rmsq_status rmsnorm_quant_mxfp4(const void* input, const void* residual, void* r
  * gs = 448 * 6 / max_{r,i} |y_ri| over the whole tensor, so that the largest block scale lands on
  * the largest E4M3 value ("rmsnorm_fp4quant" takes gs as a precomputed [1] fp32 tensor; this is
  * the step that precomputes it). Reads input (and residual) once more; writes nothing but the one
- * float. gs_out is a DEVICE pointer to one fp32; an all-zero tensor gives gs = 1.
+ * float. gs_out is a DEVICE pointer to one fp32; an all-zero tensor (or rows = 0) gives gs = 1.
+ * One kernel launch: its last CTA turns the launch's running maximum into gs, using two words of
+ * a per-launch slot of the library's scratch pool (4096 slots, taken in turn, left at zero), so
+ * launches on different streams that run at the same time stay apart unless 4096 launches apart.
  * Arguments as for rmsnorm_quant_nvfp4 (no outputs besides gs_out).
  * ------------------------------------------------------------------------------------------- */
 rmsq_status rmsnorm_nvfp4_global_scale(const void* input, const void* residual,

@@ -25,7 +25,10 @@ def _case(i):
     step = {"fp8": 8 if dtype != "fp32" else 4, "nvfp4": 16, "mxfp4": 32}[mode]
     cap = 65536 if dtype != "fp32" else 32768
     # a width from 1 to 64 blocks of step (short rows) or up to the cluster range (wide rows)
-    if rng.random() < 0.75:
+    u = rng.random()
+    if u < 0.15:
+        hidden = step * int(rng.integers(1, 9))                       # a few blocks
+    elif u < 0.75:
         hidden = step * int(rng.integers(1, 1024 // step + 2)) * int(rng.choice([1, 4, 16]))
     else:
         hidden = 256 * int(rng.integers(1, cap // 256 + 1))
@@ -38,7 +41,7 @@ def _case(i):
     return mode, dtype, residual, offset, rows, hidden, opt
 
 
-CASES = [_case(i) for i in range(48)]
+CASES = [_case(i) for i in range(96)]
 
 
 @pytest.mark.parametrize("case", CASES, ids=lambda c: "%s-%s-res%d-off%g-%dx%d-%d" % c)
