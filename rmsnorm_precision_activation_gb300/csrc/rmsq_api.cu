@@ -322,11 +322,19 @@ static bool make_plan(int mode, int dt, bool res, bool w16, int hidden, const De
             // Kernels with one exchange per row (all but FP8 with an offset or fp32 input) hold
             // two rows while their exchange is in flight, so a third slot keeps a load going:
             // measured on GB300, 8-25 % faster than two slots at 16384-131072 elements.
+            // With a residual those kernels split the slot: the ring holds x only and one more
+            // slot holds the next row's residual (its mbarrier and row number one more entry),
+            // which needs three ring slots at least.
+            const bool split = one_exchange && res;
+            const int min_stages = split ? 3 : 2;
             int stages = g_tune_stages.load();
             if (stages == 0) stages = one_exchange ? 3 : 2;
-            if (stages < 2) stages = 2;
-            auto cbytes = [&](int st) { return st * cstage + red_bytes + st * 16 + kClusterXchBytes; };
-            while (stages > 2 && cbytes(stages) > di.smem_optin) --stages;
+            if (stages < min_stages) stages = min_stages;
+            auto cbytes = [&](int st) {
+                return split ? st * (cstage / 2) + cstage / 2 + red_bytes + (st + 1) * 16 + kClusterXchBytes
+                             : st * cstage + red_bytes + st * 16 + kClusterXchBytes;
+            };
+            while (stages > min_stages && cbytes(stages) > di.smem_optin) --stages;
             pl.sched = SCHED_CLUSTER;
             pl.cluster = best;
             pl.vpt = cv;
@@ -383,7 +391,7 @@ static bool make_plan(int mode, int dt, bool res, bool w16, int hidden, const De
         // shared memory
         auto ctas = [&](int st) {
             long long c = pl.ctas_per_sm;
-            constexpr int regs = reg_cap<DT_FP16, MODE_FP8, 4, SCHED_PIPE, false>();
+            constexpr int regs = reg_cap<DT_FP16, true, MODE_FP8, 4, SCHED_PIPE, false>();
             const long long by_regs = (65536 / (regs * 32)) / (threads / 32);
             const long long by_smem = di.smem_per_sm / (bytes(st) + di.smem_reserved);
             if (by_regs < c) c = by_regs;

@@ -836,18 +836,21 @@ __host__ __device__ constexpr bool fp8_offset16()
     return MODE == MODE_FP8 && !W16 && DT != DT_F32 && VPT == 4 && SCHED != SCHED_CLUSTER;
 }
 
-// Registers per thread: those kernels are capped at 80 so that three CTAs of 256 threads fit an
-// SM (measured on GB300: the cap costs no spills there); the rest take what 512 threads allow.
-template <int DT, int MODE, int VPT, int SCHED, bool W16>
+// Registers per thread: those kernels, and the cluster-schedule kernels of 16-bit rows with a
+// residual and four vectors per thread, are capped at 80 so that three CTAs of 256 threads fit
+// an SM (the cap costs no spills there); the rest take what 512 threads allow.
+template <int DT, bool RES, int MODE, int VPT, int SCHED, bool W16>
 __host__ __device__ constexpr int reg_cap()
 {
-    return fp8_offset16<DT, MODE, VPT, SCHED, W16>() ? 80 : 128;
+    return fp8_offset16<DT, MODE, VPT, SCHED, W16>() || (SCHED == SCHED_CLUSTER && RES && W16 && VPT == 4)
+               ? 80
+               : 128;
 }
 
 // W16: 16-bit input with weight_offset 0, so w = gamma is a 16-bit value and s * w, s^2 are
 // exact products formed straight from packed halves by mixed-precision FMA (no unpacking).
 template <int DT, bool RES, int MODE, int VPT, int SCHED, bool W16>
-__global__ void __launch_bounds__(512, 1) __maxnreg__((reg_cap<DT, MODE, VPT, SCHED, W16>()))
+__global__ void __launch_bounds__(512, 1) __maxnreg__((reg_cap<DT, RES, MODE, VPT, SCHED, W16>()))
 rmsq_row_kernel(const Params p)
 {
     using E = Elem<DT>;
@@ -886,6 +889,11 @@ rmsq_row_kernel(const Params p)
     // SCHED_CLUSTER with one exchange per row (every kernel that keeps s in its slot): the
     // exchange of a row overlaps the first pass of the next one (see the row loop).
     constexpr bool PIPE_X = CLUSTER && SMEM_S;
+    // PIPE_X with a residual: the ring's slots hold x only (x becomes s and must live until its
+    // row is finished, one row later), and the residual has a one-slot ring of its own, refilled
+    // with the next row's residual as soon as the first pass is over. Two rows held plus one
+    // loading then cost 3 x-slots + 1 residual slot instead of 3 slots of both.
+    constexpr bool SPLIT_RES = PIPE_X && RES;
 
     extern __shared__ __align__(128) unsigned char smem[];
 
@@ -903,24 +911,28 @@ rmsq_row_kernel(const Params p)
     const long long stride = p.nvec;                                      // vectors per row
     const int voff = static_cast<int>(crank) * nv;
     const uint32_t row_bytes = static_cast<uint32_t>(nv) * 16u;
-    const uint32_t stage_bytes = row_bytes * (RES ? 2u : 1u);
+    const uint32_t stage_bytes = row_bytes * (RES && !SPLIT_RES ? 2u : 1u);
     const int S = RING ? p.stages : 0;
     const int nrings = WARP_ROWS ? nwarps : 1;
-
-    float* red = reinterpret_cast<float*>(smem + static_cast<size_t>(S) * nrings * stage_bytes);
+    // SPLIT_RES: the residual slot follows the ring; its mbarrier and row number are entry S of
+    // the (then S + 1 long) barrier and row arrays
+    const uint32_t rslot_bytes = SPLIT_RES ? row_bytes : 0u;
+    const int SB = S + (SPLIT_RES ? 1 : 0);
+    float* red = reinterpret_cast<float*>(smem + static_cast<size_t>(S) * nrings * stage_bytes + rslot_bytes);
     float2* red_ss_all = reinterpret_cast<float2*>(red);                    // [2][32]
     float* red_max_all = red + 128;                                         // [2][32]
     float* nv_factor = WARP_ROWS ? red : red + 192;                         // [128]
 
     uint64_t* bars_all =
         reinterpret_cast<uint64_t*>(red + (WARP_ROWS ? kRedFloatsWarp : kRedFloats));  // [nrings][S]
-    long long* rows_all = reinterpret_cast<long long*>(bars_all + S * nrings);        // [nrings][S]
+    long long* rows_all = reinterpret_cast<long long*>(bars_all + SB * nrings);       // [nrings][SB]
     // this thread's ring: its slots, its mbarriers, the row of each slot (-1: the ring is done),
     // the thread that refills it, and its rows
     unsigned char* ring = smem + (WARP_ROWS ? static_cast<size_t>(warp) * S * stage_bytes : 0);
     uint64_t* bars = bars_all + (WARP_ROWS ? warp * S : 0);
     long long* slot_rows = rows_all + (WARP_ROWS ? warp * S : 0);
-    float4* xch = reinterpret_cast<float4*>(rows_all + S * nrings);                  // [4]
+    float4* xch = reinterpret_cast<float4*>(rows_all + SB * nrings);                 // [4]
+    const uint32_t rslot = smem_u32(smem + static_cast<size_t>(S) * stage_bytes);   // SPLIT_RES
     const bool issuer = WARP_ROWS ? lane == 0 : tid == 0;
     const long long row0 = WARP_ROWS ? static_cast<long long>(blockIdx.x) * nwarps + warp
                            : CLUSTER ? static_cast<long long>(cluster_id())
@@ -939,7 +951,7 @@ rmsq_row_kernel(const Params p)
     if constexpr (RING) {
         policy = l2_evict_normal_policy();
         if (issuer) {
-            for (int s = 0; s < S; ++s) mbar_init(smem_u32(&bars[s]), 1);
+            for (int s = 0; s < SB; ++s) mbar_init(smem_u32(&bars[s]), 1);
             fence_mbar_init();
         }
     }
@@ -1005,13 +1017,33 @@ rmsq_row_kernel(const Params p)
         if (reuse) fence_proxy_async_smem();
         mbar_arrive_expect_tx(bar, stage_bytes);
         bulk_load(addr, xg + r * stride, row_bytes, bar, policy);
-        if constexpr (RES) bulk_load(addr + row_bytes, rg + r * stride, row_bytes, bar, policy);
+        if constexpr (RES && !SPLIT_RES) bulk_load(addr + row_bytes, rg + r * stride, row_bytes, bar, policy);
+    };
+    // SPLIT_RES: load row r's residual into the residual slot (r < 0: complete its phase empty).
+    // Every acquisition of a ring slot pairs with one phase of the residual slot, in ring order.
+    bool r_pending = false;       // (issuer) a residual phase not yet seen complete, and its parity
+    uint32_t r_pend_par = 0;
+    uint32_t rparity = 0;         // the residual slot's next phase parity (every thread)
+    auto refill_res = [&](long long r, bool reuse) {
+        const uint32_t bar = smem_u32(&bars[S]);
+        slot_rows[S] = r;
+        if (r < 0) {
+            mbar_arrive(bar);
+        } else {
+            if (reuse) fence_proxy_async_smem();
+            mbar_arrive_expect_tx(bar, row_bytes);
+            bulk_load(rslot, rg + r * stride, row_bytes, bar, policy);
+        }
+        r_pending = true;
+        r_pend_par = rparity;
     };
     if constexpr (RING) {
         // the ring's first rows, issued by the thread that initialised its barriers
-        if (issuer)
+        if (issuer) {
             for (int s = 0; s < S; ++s)
                 refill(s, smem_u32(ring + static_cast<size_t>(s) * stage_bytes), false);
+            if constexpr (SPLIT_RES) refill_res(slot_rows[0], false);
+        }
     }
 
     float gs = 1.0f, gs_over_6 = 0.0f;
@@ -1070,6 +1102,13 @@ rmsq_row_kernel(const Params p)
         if constexpr (RING) {
             stage_addr = smem_u32(ring + static_cast<size_t>(stage) * stage_bytes);
             timed_out = !mbar_wait_bounded(smem_u32(&bars[stage]), parity, p.timeout_ns);
+            if constexpr (SPLIT_RES) {
+                // this acquisition's phase of the residual slot (empty when the slot is)
+                const bool rok = mbar_wait_bounded(smem_u32(&bars[S]), rparity, p.timeout_ns);
+                timed_out = timed_out || !rok;
+                if (rok) r_pending = false;
+                rparity ^= 1u;
+            }
             // The slot's row number was written before its barrier was armed, and an empty slot
             // (-1) completes at once, so every thread of the ring reads the same value here.
             row = slot_rows[stage];
@@ -1103,7 +1142,8 @@ rmsq_row_kernel(const Params p)
                 uint4 xv, rv;
                 if constexpr (RING) {
                     xv = ld_shared_v4(stage_addr + v * 16u);
-                    if constexpr (RES) rv = ld_shared_v4(stage_addr + row_bytes + v * 16u);
+                    if constexpr (SPLIT_RES) rv = ld_shared_v4(rslot + v * 16u);
+                    else if constexpr (RES) rv = ld_shared_v4(stage_addr + row_bytes + v * 16u);
                 } else {
                     xv = ld_stream_v4(xrow + v);
                     if constexpr (RES) rv = ld_stream_v4(rrow + v);
@@ -1226,6 +1266,11 @@ rmsq_row_kernel(const Params p)
         };
         if constexpr (WARP_ROWS) stop = __any_sync(0xFFFFFFFFu, timed_out);
         else stop = __syncthreads_or(timed_out);
+        if constexpr (SPLIT_RES) {
+            // every thread is past its reads of the residual slot: load the next acquisition's
+            // residual now (not after a timed-out wait: the CTA stops below)
+            if (issuer && !stop) refill_res(slot_rows[stage], true);
+        }
         // the row's (or, for SCHED_CLUSTER, this CTA's slice's) sum of squares and ONE_BAR max,
         // the same in every thread
         FF tot = ss;
@@ -1342,6 +1387,10 @@ rmsq_row_kernel(const Params p)
                         n = S - 1;
                     }
                     bool drained = true;
+                    if constexpr (SPLIT_RES) {
+                        if (r_pending)
+                            drained = mbar_wait_bounded(smem_u32(&bars[S]), r_pend_par, 4 * p.timeout_ns);
+                    }
                     for (int j = 0; j < n; ++j) {
                         drained = mbar_wait_bounded(smem_u32(&bars[js]), jp, 4 * p.timeout_ns) && drained;
                         if (++js == S) {
