@@ -1358,8 +1358,12 @@ rmsq_row_kernel(const Params p)
                 pend_addr = next_addr;
                 pend_cslot = my_cslot;
             } else {
+                // As above, only the slot writer arrives with release semantics; the others'
+                // reads of earlier slots were consumed (the stop decision, the row's scale)
+                // before they arrive again.
                 if (tid == 0) *slot = make_float4(tot.hi, tot.lo, tmax, stop ? 1.0f : 0.0f);
-                cluster_sync();
+                cluster_arrive_as(tid == 0);
+                cluster_wait();
                 gather(slot);
             }
         }
@@ -1498,7 +1502,8 @@ rmsq_row_kernel(const Params p)
                     float4* slot = &xch[3 + mpar];
                     mpar ^= 1;
                     if (tid == 0) *slot = make_float4(amax, 0.0f, 0.0f, 0.0f);
-                    cluster_sync();
+                    cluster_arrive_as(tid == 0);
+                    cluster_wait();
                     float mx = 0.0f;
                     for (uint32_t k = 0; k < csize; ++k) mx = fmaxf(mx, ld_cluster_f4(smem_u32(slot), k).x);
                     amax = mx;
