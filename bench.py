@@ -824,6 +824,9 @@ def next_row_cases():
         ("NEXT-4", "cluster_rows", wide("fp8", 2048, 131072), {}),
         ("NEXT-4", "cluster_rows", wide("nvfp4", 2048, 131072), {}),
         ("NEXT-4", "cluster_rows", wide("mxfp4", 2048, 131072), {}),
+        ("NEXT-4", "cluster_rows_offset", W.config("fp8_gemma", rows=4096, hidden=65536), {}),
+        ("NEXT-4", "cluster_rows_no_residual", W.Workload("wide_rows", "fp8", 4096, 65536, "bf16",
+                                                          False, scale_ub=1200.0), {}),
     ]
 
 
@@ -912,7 +915,7 @@ def run_report_next(args):
             line["base_us"] = round(_time_launch(launcher(w, db, {}), flush, args.report_reps), 2)
             line["base"] = "%s input" % w.dtype
             del db
-        elif case != "cluster_rows":
+        elif not case.startswith("cluster_rows"):
             line["base_us"] = round(_time_launch(launcher(w, d, {}), flush, args.report_reps), 2)
             line["base"] = {"swizzled_scales": "row-major scales",
                             "global_scale_prepass": "the NVFP4 quantiser on the same input",

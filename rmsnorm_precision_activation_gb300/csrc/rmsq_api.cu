@@ -276,7 +276,7 @@ static bool make_plan(int mode, int dt, bool res, bool w16, int hidden, const De
     // (three CTAs per SM, so one CTA's row-end barrier and exchange overlap the others' work;
     // measured on GB300: 4.5-5.1 TB/s against 3.7-4.5 TB/s with one CTA per SM at 32768), else
     // the smallest whose ring fits; slices hold whole FP4 scale blocks; 4 or 8 vectors per
-    // thread, at most 256 threads (FP8: 512).
+    // thread (below).
     const int red_bytes = kRedFloats * 4;
     const bool pipe_fits = 2 * stage + red_bytes + 2 * 16 <= di.smem_optin;
     // A CTA covers at most 512 threads x 8 vectors: wider rows take a cluster even when two of
@@ -301,22 +301,29 @@ static bool make_plan(int mode, int dt, bool res, bool w16, int hidden, const De
             }
         }
         const bool one_exchange = mode != MODE_FP8 || w16;
-        if (best == 16 && mode == MODE_FP8 && one_exchange && tune_c == 0 && nv % 8 == 0) {
-            // FP8 split 8 ways with a three-slot ring (one CTA per SM) measured faster on GB300
-            // than 16 ways (545 against 584-750 us at 2048 x 131072 with a residual)
-            const long long s8 = static_cast<long long>(nv / 8) * 16 * (res ? 2 : 1);
-            if (3 * s8 + red_bytes + 3 * 16 + kClusterXchBytes <= di.smem_optin) best = 8;
-        }
         if (best != 0) {
             const int nvc = nv / best;
             const long long cstage = static_cast<long long>(nvc) * 16 * (res ? 2 : 1);
-            // (FP8: up to 512 threads with 4 vectors each; measured on GB300 at 2048 x 131072,
-            // 484 us against 529 us with 8 vectors and 256 threads)
+            // Vectors per thread (instantiated for 4 and 8). FP8 and NVFP4 with 16-bit input: 8,
+            // so a CTA has half the threads and twice as many fit an SM beside the others of
+            // their cluster. Measured on GB300 against 4:
+            //  - FP8 without a residual: 283 against 453 us at 2048 x 131072, 263 against 353 us
+            //    at 4096 x 65536;
+            //  - FP8 with a weight offset: 666 against 811 us at 2048 x 131072, 489 against
+            //    507 us at 4096 x 65536;
+            //  - clusters of 16 with a residual: FP8 470 against 488 us, NVFP4 314 against
+            //    347 us (2048 x 131072);
+            //  - within 2 % of 4 on the other shapes, except the W16 FP8 kernel with a residual
+            //    in clusters of 2 or 4, which keeps 4 (320 against 324 us at 8192 x 32768).
+            // MXFP4 and fp32 input: 4, or 8 when that would take more than 256 threads (FP8: 512);
+            // 8 measured slower for MXFP4 (422 against 373 us at 2048 x 131072).
             int cv = g_tune_vpt.load();
-            if (cv < 4 || (nvc + cv - 1) / cv > 512) {        // instantiated for 4 and 8
+            if (cv < 4 || (nvc + cv - 1) / cv > 512) {
                 cv = 4;
                 const int per = mode == MODE_FP8 ? 512 : 256;
                 while (cv < 8 && nvc > per * cv) cv *= 2;
+                const bool small_w16_res = mode == MODE_FP8 && w16 && res && best < 8;
+                if ((mode == MODE_FP8 || mode == MODE_NVFP4) && dt != DT_F32 && !small_w16_res) cv = 8;
             }
             // ring slots, reduction area, per slot an mbarrier and a row number, exchange slots.
             // Kernels with one exchange per row (all but FP8 with an offset or fp32 input) hold

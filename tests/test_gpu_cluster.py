@@ -162,3 +162,36 @@ def test_cluster_ring_depth_leaves_every_bit(mode):
         assert all(torch.equal(a, b) for a, b in zip(got, ref)), stages
     _check(mode, w, d)
     assert rq().rmsq_device_status() == 0
+
+
+class vectors_per_thread:
+    def __init__(self, v):
+        self.v = v
+
+    def __enter__(self):
+        rq().rmsq_set_tuning(0, 0, self.v)
+
+    def __exit__(self, *exc):
+        rq().rmsq_set_tuning(0, 0, 0)
+
+
+@pytest.mark.parametrize("vpt", [4, 8])
+@pytest.mark.parametrize("case", ["fp8_bf16_res", "fp8_bf16", "fp8_fp16_offset", "nvfp4_bf16_res",
+                                  "mxfp4_bf16_res", "fp8_fp32_res"])
+def test_cluster_both_vector_widths(case, vpt):
+    # The planner gives 16-bit FP8 and NVFP4 slices 8 vectors per thread and the rest 4 (8 on
+    # slices wider than 1024 vectors); both widths of every kernel stay checked, on wide rows
+    # (automatic cluster) and on narrow rows with every forced cluster size.
+    mode = case.split("_")[0]
+    dtype = {"bf16": torch.bfloat16, "fp16": torch.float16, "fp32": torch.float32}[case.split("_")[1]]
+    res = case.endswith("res") or case.endswith("offset")
+    off = 1.0 if case.endswith("offset") else 0.0
+    wide = 65536 if dtype == torch.float32 else 131072
+    ww = W.Workload("custom", mode, 23, wide, "bf16", res, weight_offset=off, scale_ub=10.0)
+    with vectors_per_thread(vpt):
+        _check(mode, ww, inputs(ww, seed=vpt + len(case), dtype=dtype))
+        for c in (2, 4, 8, 16):
+            w = W.Workload("custom", mode, 97, 8192, "bf16", res, weight_offset=off, scale_ub=10.0)
+            with schedule(CLUSTER), cluster_size(c):
+                _check(mode, w, inputs(w, seed=c * 7 + vpt, dtype=dtype))
+    assert rq().rmsq_device_status() == 0
