@@ -251,6 +251,42 @@ rmsq_status rmsq_debug_convert(int fmt, const float* in, uint8_t* out, int64_t n
 /* Kernel launches issued by this library in this process (for launch accounting). */
 uint64_t rmsq_launch_count(void);
 
+/* ---------------------------------------------------------------------------------------------
+ * rmsq_plan -- the launch plan an entry point would choose now for rows of `hidden` elements:
+ * schedule, vectors per thread, CTA size, ring depth, cluster size and shared memory, tuning
+ * settings included (the same planner the entry points call). A diagnostic; it launches nothing.
+ *
+ *   mode           0 = rmsnorm_quant_fp8, 1 = rmsnorm_quant_nvfp4, 2 = rmsnorm_quant_mxfp4,
+ *                  3 = rmsnorm_nvfp4_global_scale
+ *   dtype, residual (0 or 1), weight_offset, hidden   as in the entry points
+ *   smem_optin, smem_per_sm, smem_reserved   the device's shared-memory limits in bytes: the
+ *                  opt-in maximum per CTA, the total per SM and the part reserved per CTA
+ *                  (cudaDevAttrMaxSharedMemoryPerBlockOptin, ...PerMultiprocessor,
+ *                  cudaDevAttrReservedSharedMemoryPerBlock; GB300: 232448, 233472, 1024), so the
+ *                  plan can be computed without a GPU; smem_optin = 0 takes the current device's
+ *   out            receives the plan (caller-owned host memory)
+ *
+ * Returns RMSQ_ERR_NULL for a NULL out; RMSQ_ERR_DTYPE or RMSQ_ERR_SHAPE as the entry point would
+ * for this dtype and width (RMSQ_ERR_SHAPE also for a tuning setting that no plan can honour);
+ * RMSQ_ERR_VALUE for an unknown mode, a weight_offset that is not finite or inconsistent limits;
+ * RMSQ_ERR_DEVICE when smem_optin = 0 and there is no usable device. The grid (resident CTAs or
+ * clusters) is sized at launch from the occupancy API and is not part of the plan.
+ * ------------------------------------------------------------------------------------------- */
+typedef struct {
+    int schedule;            /* 1 CTA per row (bulk-copy ring), 2 register rows, 3 row per warp,
+                                4 cluster per row (the values of rmsq_set_schedule) */
+    int vectors_per_thread;  /* 16-byte vectors per thread of each row (cluster: of each slice) */
+    int threads;             /* threads per CTA */
+    int stages;              /* ring slots per CTA (row per warp: per warp; 0 for schedule 2) */
+    int cluster;             /* CTAs per cluster (1 unless schedule 4) */
+    int smem_bytes;          /* dynamic shared memory per CTA */
+    int ctas_per_sm;         /* cap on resident CTAs per SM (0: the occupancy limit) */
+    int w16;                 /* 1: 16-bit input with weight_offset 0 (exact packed products) */
+} rmsq_plan_info;
+
+rmsq_status rmsq_plan(int mode, int dtype, int residual, float weight_offset, int64_t hidden,
+                      int smem_optin, int smem_per_sm, int smem_reserved, rmsq_plan_info* out);
+
 #ifdef __cplusplus
 }
 #endif

@@ -53,7 +53,18 @@ SIGNATURES = {
     "rmsq_selftest_wait_timeout": ([_U64, _P], _I),
     "rmsq_debug_convert": ([_I, _P, _P, _I64, _P], _I),
     "rmsq_launch_count": ([], _U64),
+    "rmsq_plan": ([_I, _I, _I, _F, _I64, _I, _I, _I, _P], _I),
 }
+
+# rmsq_plan's modes, and GB300's shared-memory limits in bytes (opt-in per CTA, per SM, reserved
+# per CTA), which let it plan without a GPU.
+MODES = {"fp8": 0, "nvfp4": 1, "mxfp4": 2, "global_scale": 3}
+GB300_SMEM = (232448, 233472, 1024)
+
+
+class PlanInfo(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int) for n in ("schedule", "vectors_per_thread", "threads", "stages",
+                                            "cluster", "smem_bytes", "ctas_per_sm", "w16")]
 
 _lib = None
 
@@ -275,3 +286,17 @@ def rmsq_debug_convert(fmt: int, values: torch.Tensor, stream=None) -> torch.Ten
 
 def rmsq_launch_count() -> int:
     return lib().rmsq_launch_count()
+
+
+def rmsq_plan(mode: str, dtype, hidden: int, residual: bool = False, weight_offset: float = 0.0,
+              smem=GB300_SMEM) -> dict:
+    """The launch plan the entry point of `mode` ("fp8", "nvfp4", "mxfp4", "global_scale") would
+    choose now for rows of `hidden` elements, tuning settings included (rmsq_plan in
+    include/rmsq.h). smem: the (opt-in per CTA, per SM, reserved per CTA) shared-memory limits in
+    bytes, GB300's by default; None takes the current device's."""
+    dt = _DT[dtype] if isinstance(dtype, torch.dtype) else int(dtype)
+    optin, per_sm, reserved = smem if smem is not None else (0, 0, 0)
+    info = PlanInfo()
+    _check(lib().rmsq_plan(MODES[mode], dt, int(bool(residual)), float(weight_offset), int(hidden),
+                           optin, per_sm, reserved, ctypes.byref(info)), "rmsq_plan")
+    return {n: getattr(info, n) for n, _ in PlanInfo._fields_}

@@ -834,3 +834,42 @@ extern "C" rmsq_status rmsq_debug_convert(int fmt, const float* in, uint8_t* out
 }
 
 extern "C" uint64_t rmsq_launch_count(void) { return g_launches.load(); }
+
+extern "C" rmsq_status rmsq_plan(int mode, int dtype, int residual, float weight_offset,
+                                 int64_t hidden, int smem_optin, int smem_per_sm, int smem_reserved,
+                                 rmsq_plan_info* out)
+{
+    if (!out) return RMSQ_ERR_NULL;
+    if (mode < MODE_FP8 || mode > MODE_AMAX) return RMSQ_ERR_VALUE;
+    // the entry point's own checks of dtype, width and weight_offset (rows = 0: no pointers)
+    const int min_multiple = mode == MODE_FP8 ? (dtype == RMSQ_F32 ? 4 : 8)
+                             : mode == MODE_MXFP4 ? 32 : 16;
+    bool empty;
+    rmsq_status st = check_common(nullptr, nullptr, nullptr, nullptr, 0, hidden, dtype, 0.0f,
+                                  weight_offset, min_multiple, &empty);
+    if (st != RMSQ_OK) return st;
+    DeviceInfo di;
+    if (smem_optin == 0) {
+        const DeviceInfo* cur = device_info();
+        if (!cur) return RMSQ_ERR_DEVICE;
+        di = *cur;
+    } else {
+        if (smem_optin < 0 || smem_per_sm < smem_optin || smem_reserved < 0) return RMSQ_ERR_VALUE;
+        di.smem_optin = smem_optin;
+        di.smem_per_sm = smem_per_sm;
+        di.smem_reserved = smem_reserved;
+    }
+    Plan pl;
+    const bool w16 = dtype != DT_F32 && weight_offset == 0.0f;
+    if (!make_plan(mode, dtype, residual != 0, w16, static_cast<int>(hidden), di, pl))
+        return RMSQ_ERR_SHAPE;
+    out->schedule = pl.sched;
+    out->vectors_per_thread = pl.vpt;
+    out->threads = pl.threads;
+    out->stages = pl.stages;
+    out->cluster = pl.sched == SCHED_CLUSTER ? pl.cluster : 1;
+    out->smem_bytes = pl.smem;
+    out->ctas_per_sm = pl.ctas_per_sm;
+    out->w16 = w16 ? 1 : 0;
+    return RMSQ_OK;
+}
