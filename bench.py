@@ -256,8 +256,13 @@ class Step:
         self.step_bytes = sum(self.bytes.values())
         self.step_rows = sum(w.rows for w in self.workloads.values())
 
-    def launch(self, mode, stream=None):
+    def launch(self, mode, stream=None, rows=None):
+        """Queue mode's kernel on its batch, or on rows [r0, r1) of it (rows=(r0, r1))."""
         d, o, w, rq = self.batches[mode], self.out[mode], self.workloads[mode], self.rq
+        if rows is not None:
+            r0, r1 = rows
+            d = {k: (v if v is None or k == "gamma" else v[r0:r1]) for k, v in d.items()}
+            o = tuple(None if t is None else t[r0:r1] for t in o)
         if mode == "fp8":
             rq.rmsnorm_quant_fp8(d["input"], d["gamma"], residual=d["residual"], residual_output=o[2],
                                  epsilon=w.eps, weight_offset=w.weight_offset, scale_ub=w.scale_ub,
@@ -438,16 +443,32 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
+E2E_CHUNK_BYTES = 512 << 20
+
+
+def e2e_chunks(w, chunk_bytes=E2E_CHUNK_BYTES, row_align=16):
+    """Row ranges [r0, r1) that split workload w's batch into pieces of about chunk_bytes of
+    input each. Every piece starts on a multiple of row_align rows, so the pointers an entry
+    point gets for it stay 16-byte aligned (an FP8 row scale is 4 bytes, or 2)."""
+    per_row = w.hidden * torch.tensor([], dtype=w.torch_dtype).element_size() * (2 if w.residual else 1)
+    n = max(1, min(w.rows, -(-w.rows * per_row // chunk_bytes)))
+    bounds = [w.rows * i // n // row_align * row_align for i in range(n)] + [w.rows]
+    return [(a, b) for a, b in zip(bounds, bounds[1:]) if b > a]
+
+
 def run_e2e(step, device, K, world):
     """Same step through the public API, inputs from pinned host memory and outputs back to
     pinned host memory inside the timed region.
 
     The batches move through three streams, the way a caller overlaps transfers with compute:
-    one stream copies each batch's inputs in (pinned host -> device), the launch stream runs the
-    kernels, and one stream copies each batch's outputs back (device -> pinned host). Events
-    order each batch's copy-in, kernel and copy-out. They also stop a copy-in from overwriting
-    inputs that batch's previous kernel still reads, and a kernel from overwriting outputs that
-    are still being copied out."""
+    one stream copies inputs in (pinned host -> device), the launch stream runs the kernels, and
+    one stream copies outputs back (device -> pinned host). Each batch goes in row chunks of
+    about 512 MB of input (rows are independent, so a chunk is one call of the entry point on
+    those rows): a chunk's kernel starts once its rows are in, and its outputs leave while the
+    next chunk comes in, so the link is busy in both directions from the first chunk to the
+    last. Events order each chunk's copy-in, kernel and copy-out. They also stop a copy-in from
+    overwriting inputs that the chunk's previous kernel still reads, and a kernel from
+    overwriting outputs that are still being copied out."""
     modes = step.modes
 
     def pinned_like(t):
@@ -465,31 +486,37 @@ def run_e2e(step, device, K, world):
     dev_out = {m: tuple(t for t in step.out[m] if t is not None) for m in modes}
     h2d = sum(t.numel() * t.element_size() for d in host_in.values() for t in d.values())
     d2h = sum(t.numel() * t.element_size() for o in host_out.values() for t in o)
+    chunks = [(m, r0, r1) for m in modes for r0, r1 in e2e_chunks(step.workloads[m])]
     compute = torch.cuda.current_stream(device)
     s_in, s_out = torch.cuda.Stream(device), torch.cuda.Stream(device)
-    in_done = {m: torch.cuda.Event() for m in modes}
-    ker_done = {m: torch.cuda.Event() for m in modes}
-    out_done = {m: torch.cuda.Event() for m in modes}
-    for m in modes:
-        ker_done[m].record(compute)
-        out_done[m].record(compute)
+    in_done = {c: torch.cuda.Event() for c in chunks}
+    ker_done = {c: torch.cuda.Event() for c in chunks}
+    out_done = {c: torch.cuda.Event() for c in chunks}
+    for c in chunks:
+        ker_done[c].record(compute)
+        out_done[c].record(compute)
 
     def one():
-        for m in modes:
-            s_in.wait_event(ker_done[m])
+        for c in chunks:
+            m, r0, r1 = c
+            s_in.wait_event(ker_done[c])
             with torch.cuda.stream(s_in):
                 for k, t in host_in[m].items():
-                    step.batches[m][k].copy_(t, non_blocking=True)
-            in_done[m].record(s_in)
-            compute.wait_event(in_done[m])
-            compute.wait_event(out_done[m])
-            step.launch(m, stream=compute)
-            ker_done[m].record(compute)
-            s_out.wait_event(ker_done[m])
+                    if k == "gamma":
+                        if r0 == 0:
+                            step.batches[m][k].copy_(t, non_blocking=True)
+                    else:
+                        step.batches[m][k][r0:r1].copy_(t[r0:r1], non_blocking=True)
+            in_done[c].record(s_in)
+            compute.wait_event(in_done[c])
+            compute.wait_event(out_done[c])
+            step.launch(m, stream=compute, rows=(r0, r1))
+            ker_done[c].record(compute)
+            s_out.wait_event(ker_done[c])
             with torch.cuda.stream(s_out):
                 for dst, src in zip(host_out[m], dev_out[m]):
-                    dst.copy_(src, non_blocking=True)
-            out_done[m].record(s_out)
+                    dst[r0:r1].copy_(src[r0:r1], non_blocking=True)
+            out_done[c].record(s_out)
 
     one()
     torch.cuda.synchronize()

@@ -101,3 +101,25 @@ def test_next_row_bytes(case):
         import rmsnorm_precision_activation_gb300 as rq
         block = 16 if w.mode == "nvfp4" else 32
         assert rq.swizzled_scale_numel(w.rows, w.hidden, block) == w.rows * w.hidden // block
+
+
+@pytest.mark.parametrize("name,rows,hidden", [("fp8_gemma", 16384, 8192), ("nvfp4", 32768, 7168),
+                                              ("mxfp4_residual", 65536, 16384),
+                                              ("mxfp4_residual", 1, 2048), ("fp8_small", 64, 4096)])
+@pytest.mark.parametrize("chunk_bytes", [1 << 20, 64 << 20, bench.E2E_CHUNK_BYTES])
+def test_e2e_chunks_cover_every_row_once(name, rows, hidden, chunk_bytes):
+    w = W.config(name, rows=rows, hidden=hidden)
+    ch = bench.e2e_chunks(w, chunk_bytes)
+    assert ch[0][0] == 0 and ch[-1][1] == rows
+    assert all(a[1] == b[0] for a, b in zip(ch, ch[1:]))        # contiguous, in order
+    assert all(r1 > r0 for r0, r1 in ch)
+    per_row = hidden * w.torch_dtype.itemsize * (2 if w.residual else 1)
+    # every piece starts on a multiple of 16 rows (16-byte aligned row scales); the fewest
+    # pieces of at most chunk_bytes on average, each within 16 rows of an even split
+    assert all(r0 % 16 == 0 for r0, _ in ch)
+    n = min(rows, -(-rows * per_row // chunk_bytes))
+    assert len(ch) <= n
+    sizes = [r1 - r0 for r0, r1 in ch]
+    assert all(k * per_row <= chunk_bytes + 16 * per_row for k in sizes)
+    if rows >= 16 * n:
+        assert len(ch) == n and max(sizes) - min(sizes) <= 16

@@ -75,3 +75,33 @@ def test_bench_step_launches_match_oracle():
     del step
     torch.cuda.empty_cache()
     assert rq().rmsq_device_status() == 0
+
+
+def test_row_chunks_equal_the_whole_batch():
+    # bench.py's end-to-end leg queues each batch as row chunks (one entry-point call per chunk,
+    # between the copies in and out); the outputs must be those of one call on the whole batch
+    import bench
+    import workloads as W
+    dev = torch.device("cuda", 0)
+    wl = {"fp8": W.config("fp8_gemma", rows=3001), "nvfp4": W.config("nvfp4", rows=2999),
+          "mxfp4": W.config("mxfp4_residual", rows=3003, hidden=16384)}
+    step = bench.Step(rq(), dev, workloads=wl, seed=5)
+    for m in step.modes:
+        step.launch(m)
+    torch.cuda.synchronize()
+    whole = {m: [None if t is None else t.view(torch.uint8).clone() for t in step.out[m]]
+             for m in step.modes}
+    for m in step.modes:
+        for t in step.out[m]:
+            if t is not None:
+                t.view(torch.uint8).fill_(0xA5)
+        chunks = bench.e2e_chunks(step.workloads[m], 8 << 20)
+        assert len(chunks) > 2, m
+        for r0, r1 in chunks:
+            step.launch(m, rows=(r0, r1))
+    torch.cuda.synchronize()
+    for m in step.modes:
+        for a, b in zip(step.out[m], whole[m]):
+            if a is not None:
+                assert torch.equal(a.view(torch.uint8), b), m
+    assert rq().rmsq_device_status() == 0
