@@ -212,11 +212,14 @@ rmsq_status rmsq_device_status(void);
  *                    (each CTA takes a slice through its own ring; the slices' sums meet in
  *                    distributed shared memory). Returns the previous value. A forced schedule
  *                    that does not fit the row falls back to the automatic choice.
- * rmsq_set_tuning    overrides the pipeline depth (stages, 0 = automatic), CTAs per SM
- *                    (0 = automatic) and vectors of 16 bytes per thread per row (0 = automatic;
- *                    1, 2, 4 or 8). Returns RMSQ_ERR_VALUE for values out of range; a setting
- *                    that needs more than 512 threads per CTA makes later calls fail with
- *                    RMSQ_ERR_SHAPE.
+ * rmsq_set_tuning    overrides the pipeline depth (stages, 0 = automatic, at most 8), CTAs per
+ *                    SM (0 = automatic, at most 32) and vectors of 16 bytes per thread per row
+ *                    (0 = automatic; 1, 2, 4 or 8). One stage is honoured by the kernels that
+ *                    refill their slot before the row ends (FP8 with a weight offset or fp32
+ *                    input, whose s is then held in registers); the others take their minimum of
+ *                    two (three for the pipelined cluster kernels with a residual). Returns
+ *                    RMSQ_ERR_VALUE for values out of range; a setting that needs more than 512
+ *                    threads per CTA makes later calls fail with RMSQ_ERR_SHAPE.
  * rmsq_set_row_warps  warps per CTA of the row-per-warp schedule (0 = automatic, at most 16).
  *                    Returns RMSQ_ERR_VALUE out of range.
  * rmsq_set_cluster_size  CTAs per cluster of the cluster schedule (0 = automatic, else 2, 4, 8

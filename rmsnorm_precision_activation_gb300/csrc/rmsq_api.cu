@@ -258,7 +258,7 @@ static bool make_plan(int mode, int dt, bool res, bool w16, int hidden, const De
         int warps = g_tune_warps.load();
         if (warps == 0) warps = 8;
         int stages = g_tune_stages.load();
-        if (stages == 0) stages = 2;
+        if (stages < 2) stages = 2;                 // automatic, or a single slot asked for
         auto bytes = [&](int w, int st) { return w * st * stage + warp_red + w * st * 16; };
         while (stages > 2 && bytes(warps, stages) > di.smem_optin) --stages;
         while (warps > 1 && bytes(warps, stages) > di.smem_optin) warps /= 2;
@@ -272,9 +272,10 @@ static bool make_plan(int mode, int dt, bool res, bool w16, int hidden, const De
     }
 
     // A cluster of C CTAs per row: for rows whose two-slot ring does not fit one CTA's shared
-    // memory or that need more than 512 threads (or when forced). The smallest C of 2, 4, 8, 16 whose slice slot holds at most 32 KB
-    // (three CTAs per SM, so one CTA's row-end barrier and exchange overlap the others' work;
-    // measured on GB300: 4.5-5.1 TB/s against 3.7-4.5 TB/s with one CTA per SM at 32768), else
+    // memory or that need more than 512 threads (or when forced). The smallest C of 2, 4, 8, 16
+    // whose slice slot holds at most 32 KB (64 KB for the one-slot offset FP8 kernel, below):
+    // three CTAs per SM, so one CTA's row-end barrier and exchange overlap the others' work
+    // (measured on GB300: 4.5-5.1 TB/s against 3.7-4.5 TB/s with one CTA per SM at 32768). Else
     // the smallest whose ring fits; slices hold whole FP4 scale blocks; 4 or 8 vectors per
     // thread (below).
     const int red_bytes = kRedFloats * 4;
@@ -285,6 +286,18 @@ static bool make_plan(int mode, int dt, bool res, bool w16, int hidden, const De
     if (forced == SCHED_CLUSTER || (!one_cta && forced != SCHED_REG)) {
         const int tune_c = g_tune_cluster.load();
         const int blk = mode == MODE_MXFP4 ? 32 : 16;
+        // The FP8 kernel with a weight offset and 16-bit input exchanges twice per row and keeps
+        // s in registers, so its ring is one slot, refilled right after the first exchange; its
+        // slot may then be twice as large, for half as many CTAs per row. Measured on GB300 (read
+        // flush), against clusters twice as large with two slots:
+        //  - 4096 x 65536 fp16 + residual: 377 against 481 us (clusters of 4);
+        //  - 2048 x 131072: 420 against 654 us (8);
+        //  - 8192 x 32768: 355 against 408 us (2);
+        //  - bf16 4096 x 65536: 435 against 556 us;
+        //  - 4096 x 65536 fp16 without a residual: 334.5 against 349 us (2).
+        // fp32 input (the other kernel with two exchanges) measured the same with one slot.
+        const bool offset16 = mode == MODE_FP8 && !w16 && dt != DT_F32;
+        const long long small_slot = offset16 ? 65536 : 32768;
         int best = 0;
         for (int c = 2; c <= 16; c *= 2) {
             if (tune_c != 0 && c != tune_c) continue;
@@ -295,7 +308,7 @@ static bool make_plan(int mode, int dt, bool res, bool w16, int hidden, const De
             if (2 * cstage + red_bytes + 2 * 16 + kClusterXchBytes > di.smem_optin) continue;
             if ((nvc + 7) / 8 > 512) continue;
             if (best == 0) best = c;              // smallest that fits
-            if (cstage <= 32768 || tune_c != 0) {
+            if (cstage <= small_slot || tune_c != 0) {
                 best = c;                         // smallest with a small slot
                 break;
             }
@@ -333,9 +346,11 @@ static bool make_plan(int mode, int dt, bool res, bool w16, int hidden, const De
             // slot holds the next row's residual (its mbarrier and row number one more entry),
             // which needs three ring slots at least.
             const bool split = one_exchange && res;
-            const int min_stages = split ? 3 : 2;
+            // kernels with two exchanges refill their slot right after the first (s is then in
+            // registers), so one slot is a valid ring for them
+            const int min_stages = split ? 3 : one_exchange ? 2 : 1;
             int stages = g_tune_stages.load();
-            if (stages == 0) stages = one_exchange ? 3 : 2;
+            if (stages == 0) stages = offset16 ? 1 : one_exchange ? 3 : 2;
             if (stages < min_stages) stages = min_stages;
             auto cbytes = [&](int st) {
                 return split ? st * (cstage / 2) + cstage / 2 + red_bytes + (st + 1) * 16 + kClusterXchBytes
@@ -416,6 +431,8 @@ static bool make_plan(int mode, int dt, bool res, bool w16, int hidden, const De
         pl.smem = static_cast<int>(bytes(stages));
     } else if (pl.sched == SCHED_PIPE) {
         int stages = g_tune_stages.load();
+        // kernels that keep s in the slot refill it at the end of the row: two slots at least
+        if (stages == 1 && (mode != MODE_FP8 || w16)) stages = 2;
         if (stages == 0)
             stages = (mode != MODE_FP8 && res && nv >= 2048) ? 3 : 2;
         // ring slots, reduction area, then per slot an mbarrier and the slot's row number
@@ -763,7 +780,7 @@ extern "C" int rmsq_set_schedule(int schedule)
 
 extern "C" rmsq_status rmsq_set_tuning(int stages, int ctas_per_sm, int vectors_per_thread)
 {
-    if (stages < 0 || stages > 8 || stages == 1 || ctas_per_sm < 0 || ctas_per_sm > 32 ||
+    if (stages < 0 || stages > 8 || ctas_per_sm < 0 || ctas_per_sm > 32 ||
         (vectors_per_thread != 0 && vectors_per_thread != 1 && vectors_per_thread != 2 &&
          vectors_per_thread != 4 && vectors_per_thread != 8))
         return RMSQ_ERR_VALUE;

@@ -72,7 +72,8 @@ def test_host_side_validation_without_gpu(lib):
     assert lib.rmsnorm_quant_nvfp4(A, None, None, A, 4, 64, 0, 1e-6, 0.0, None, A, A, 0, None) == 1
     assert lib.rmsnorm_quant_mxfp4(A, None, None, A, 4, 48, 0, 1e-6, 0.0, A, A, 0, None) == 2
     assert lib.rmsnorm_quant_mxfp4(A, None, None, A, 4, 64, 0, 1e-6, 0.0, A, A, 2, None) == 4
-    assert lib.rmsq_set_tuning(1, 0, 0) == 6 and lib.rmsq_set_tuning(0, 0, 3) == 6
+    assert lib.rmsq_set_tuning(9, 0, 0) == 6 and lib.rmsq_set_tuning(0, 0, 3) == 6
+    assert lib.rmsq_set_tuning(-1, 0, 0) == 6 and lib.rmsq_set_tuning(0, 33, 0) == 6
     assert lib.rmsq_set_tuning(0, 0, 0) == 0
 
 

@@ -88,3 +88,36 @@ def test_fp8_weight_offset_shapes(rows, hidden, dtype, sched):
     with schedule(sched):
         rep, _ = check_fp8(w, d)
     assert rep["bad"] == 0 and rep["tolerated"] == 0
+
+
+class _stages:
+    def __init__(self, n):
+        self.n = n
+
+    def __enter__(self):
+        from gpu_common import rq
+        rq().rmsq_set_tuning(self.n, 0, 0)
+
+    def __exit__(self, *exc):
+        from gpu_common import rq
+        rq().rmsq_set_tuning(0, 0, 0)
+
+
+@pytest.mark.parametrize("dtype,offset,hidden,residual", [
+    (torch.float32, 0.0, 8192, True),       # one CTA per row
+    (torch.float32, 0.5, 2048 + 64, False),
+    (torch.float32, 0.0, 65536, True),      # cluster
+    (torch.float16, 1.0, 8192, True),       # one CTA per row, w table
+    (torch.bfloat16, 1.0, 65536, True),     # cluster (one slot is its plan)
+    (torch.float16, 1.0, 131072, True),
+    (torch.float16, 1.0, 65536, False),
+])
+def test_fp8_one_slot_ring(dtype, offset, hidden, residual):
+    # the kernels that hold s in registers refill their slot right after the sum-of-squares
+    # barrier, so a ring of one slot is valid for them: every code and scale as the oracle's
+    w = W.Workload("custom", "fp8", 37, hidden, "bf16", residual, weight_offset=offset,
+                   scale_ub=10.0)
+    d = inputs(w, seed=hidden // 64 + int(residual), dtype=dtype)
+    with _stages(1):
+        rep, _ = check_fp8(w, d)
+    assert rep["bad"] == 0

@@ -113,8 +113,11 @@ def test_wide_rows_take_a_cluster(mode, rq):
     ("fp8", BF16, 32768, True, 0.0, 4, 4),         # W16 with a residual on a cluster of 4 keeps 4
     ("fp8", BF16, 65536, False, 0.0, 4, 8),
     ("fp8", BF16, 131072, False, 0.0, 8, 8),
-    ("fp8", FP16, 65536, True, 1.0, 8, 8),         # the offset kernel
-    ("fp8", FP16, 131072, True, 1.0, 16, 8),
+    ("fp8", FP16, 65536, True, 1.0, 4, 8),         # the offset kernel: one slot of up to 64 KB
+    ("fp8", FP16, 131072, True, 1.0, 8, 8),
+    ("fp8", FP16, 32768, True, 1.0, 2, 8),
+    ("fp8", FP16, 65536, False, 1.0, 2, 8),
+    ("fp8", BF16, 65536, True, 1.0, 4, 8),
     ("fp8", F32, 65536, True, 0.0, 16, 4),         # fp32 input keeps 4
     ("nvfp4", BF16, 65536, True, 0.0, 8, 8),
     ("nvfp4", BF16, 131072, True, 0.0, 16, 8),
@@ -129,9 +132,11 @@ def test_cluster_sizes_and_vectors(mode, dtype, hidden, res, off, cluster, vpt, 
     assert (p["cluster"], p["vectors_per_thread"]) == (cluster, vpt), p
     nvc = hidden // (8 if dtype != F32 else 4) // cluster
     assert p["threads"] == ((nvc + vpt - 1) // vpt + 31) // 32 * 32
-    # pipelined kernels (one exchange per row) keep three slots; the two-exchange ones two
+    # pipelined kernels (one exchange per row) keep three slots; the two-exchange ones two,
+    # except the offset kernel with 16-bit input, which refills its one slot after the first
     one_exchange = mode != "fp8" or (dtype != F32 and off == 0.0)
-    assert p["stages"] == (3 if one_exchange else 2)
+    offset16 = mode == "fp8" and dtype != F32 and off != 0.0
+    assert p["stages"] == (3 if one_exchange else 1 if offset16 else 2)
 
 
 def _widths(mode, dtype):
@@ -206,6 +211,19 @@ def test_tuning_settings_are_reflected(rq):
     try:
         p = plan(rq, "mxfp4", BF16, 8192, True)
         assert (p["stages"], p["vectors_per_thread"]) == (3, 2)
+    finally:
+        rq.rmsq_set_tuning(0, 0, 0)
+    # one slot: honoured where s is held in registers (FP8 with an offset or fp32 input), two or
+    # three slots at least elsewhere
+    rq.rmsq_set_tuning(1, 0, 0)
+    try:
+        assert plan(rq, "fp8", F32, 8192, True)["stages"] == 1
+        assert plan(rq, "fp8", F32, 65536, True)["stages"] == 1
+        assert plan(rq, "fp8", FP16, 8192, True, 1.0)["stages"] == 1
+        assert plan(rq, "fp8", BF16, 8192, True)["stages"] == 2
+        assert plan(rq, "mxfp4", BF16, 512, True)["stages"] == 2        # row per warp
+        assert plan(rq, "nvfp4", BF16, 65536, True)["stages"] == 3      # split residual ring
+        assert plan(rq, "nvfp4", BF16, 65536)["stages"] == 2
     finally:
         rq.rmsq_set_tuning(0, 0, 0)
     assert plan(rq, "mxfp4", BF16, 8192, True) == base
