@@ -273,7 +273,7 @@ static bool make_plan(int mode, int dt, bool res, bool w16, int hidden, const De
 
     // A cluster of C CTAs per row: for rows whose two-slot ring does not fit one CTA's shared
     // memory or that need more than 512 threads (or when forced). The smallest C of 2, 4, 8, 16
-    // whose slice slot holds at most 32 KB (64 KB for the one-slot offset FP8 kernel, below):
+    // whose slice slot holds at most 32 KB (64 KB for the one-slot FP8 kernels, below):
     // three CTAs per SM, so one CTA's row-end barrier and exchange overlap the others' work
     // (measured on GB300: 4.5-5.1 TB/s against 3.7-4.5 TB/s with one CTA per SM at 32768). Else
     // the smallest whose ring fits; slices hold whole FP4 scale blocks; 4 or 8 vectors per
@@ -286,18 +286,18 @@ static bool make_plan(int mode, int dt, bool res, bool w16, int hidden, const De
     if (forced == SCHED_CLUSTER || (!one_cta && forced != SCHED_REG)) {
         const int tune_c = g_tune_cluster.load();
         const int blk = mode == MODE_MXFP4 ? 32 : 16;
-        // The FP8 kernel with a weight offset and 16-bit input exchanges twice per row and keeps
-        // s in registers, so its ring is one slot, refilled right after the first exchange; its
+        // The FP8 kernels with two exchanges per row (a weight offset, or fp32 input) keep s in
+        // registers, so their ring is one slot, refilled right after the first exchange; the
         // slot may then be twice as large, for half as many CTAs per row. Measured on GB300 (read
-        // flush), against clusters twice as large with two slots:
-        //  - 4096 x 65536 fp16 + residual: 377 against 481 us (clusters of 4);
-        //  - 2048 x 131072: 420 against 654 us (8);
-        //  - 8192 x 32768: 355 against 408 us (2);
-        //  - bf16 4096 x 65536: 435 against 556 us;
-        //  - 4096 x 65536 fp16 without a residual: 334.5 against 349 us (2).
-        // fp32 input (the other kernel with two exchanges) measured the same with one slot.
-        const bool offset16 = mode == MODE_FP8 && !w16 && dt != DT_F32;
-        const long long small_slot = offset16 ? 65536 : 32768;
+        // flush), against two slots on clusters twice as large:
+        //  - fp16 with an offset, 4096 x 65536 + residual: 377 against 481 us (clusters of 4);
+        //    2048 x 131072: 420 against 654 us (8); 8192 x 32768: 355 against 408 us (2);
+        //    without a residual, 4096 x 65536: 334.5 against 349 us (2);
+        //  - bf16 with an offset, 4096 x 65536: 435 against 556 us;
+        //  - fp32, 2048 x 65536 + residual: 293 against 486 us (8 vectors per thread both);
+        //    4096 x 32768: 264 against 334.5 us; without a residual, 238 against 245 us.
+        const bool two_x = mode == MODE_FP8 && !w16;
+        const long long small_slot = two_x ? 65536 : 32768;
         int best = 0;
         for (int c = 2; c <= 16; c *= 2) {
             if (tune_c != 0 && c != tune_c) continue;
@@ -317,26 +317,29 @@ static bool make_plan(int mode, int dt, bool res, bool w16, int hidden, const De
         if (best != 0) {
             const int nvc = nv / best;
             const long long cstage = static_cast<long long>(nvc) * 16 * (res ? 2 : 1);
-            // Vectors per thread (instantiated for 4 and 8). FP8 and NVFP4 with 16-bit input: 8,
-            // so a CTA has half the threads and twice as many fit an SM beside the others of
-            // their cluster. Measured on GB300 against 4:
+            // Vectors per thread (instantiated for 4 and 8). FP8 and NVFP4: 8, so a CTA has half
+            // the threads and twice as many fit an SM beside the others of their cluster.
+            // Measured on GB300 against 4:
             //  - FP8 without a residual: 283 against 453 us at 2048 x 131072, 263 against 353 us
             //    at 4096 x 65536;
             //  - FP8 with a weight offset: 666 against 811 us at 2048 x 131072, 489 against
             //    507 us at 4096 x 65536;
             //  - clusters of 16 with a residual: FP8 470 against 488 us, NVFP4 314 against
             //    347 us (2048 x 131072);
+            //  - fp32 input: FP8 at 2048 x 65536 486 against 689 us, 4096 x 32768 334.5 against
+            //    400 us (two slots); NVFP4 at 2048 x 65536 322 against 339 us;
             //  - within 2 % of 4 on the other shapes, except the W16 FP8 kernel with a residual
             //    in clusters of 2 or 4, which keeps 4 (320 against 324 us at 8192 x 32768).
-            // MXFP4 and fp32 input: 4, or 8 when that would take more than 256 threads (FP8: 512);
-            // 8 measured slower for MXFP4 (422 against 373 us at 2048 x 131072).
+            // MXFP4: 4, or 8 when that would take more than 256 threads. 8 measured slower at
+            // 2048 x 131072 bf16 (422 against 373 us) and at 4096 x 32768 fp32 (317 against
+            // 298 us), faster only at 2048 x 65536 fp32 (412 against 450 us).
             int cv = g_tune_vpt.load();
             if (cv < 4 || (nvc + cv - 1) / cv > 512) {
                 cv = 4;
                 const int per = mode == MODE_FP8 ? 512 : 256;
                 while (cv < 8 && nvc > per * cv) cv *= 2;
                 const bool small_w16_res = mode == MODE_FP8 && w16 && res && best < 8;
-                if ((mode == MODE_FP8 || mode == MODE_NVFP4) && dt != DT_F32 && !small_w16_res) cv = 8;
+                if ((mode == MODE_FP8 || mode == MODE_NVFP4) && !small_w16_res) cv = 8;
             }
             // ring slots, reduction area, per slot an mbarrier and a row number, exchange slots.
             // Kernels with one exchange per row (all but FP8 with an offset or fp32 input) hold
@@ -350,7 +353,7 @@ static bool make_plan(int mode, int dt, bool res, bool w16, int hidden, const De
             // registers), so one slot is a valid ring for them
             const int min_stages = split ? 3 : one_exchange ? 2 : 1;
             int stages = g_tune_stages.load();
-            if (stages == 0) stages = offset16 ? 1 : one_exchange ? 3 : 2;
+            if (stages == 0) stages = two_x ? 1 : one_exchange ? 3 : 2;
             if (stages < min_stages) stages = min_stages;
             auto cbytes = [&](int st) {
                 return split ? st * (cstage / 2) + cstage / 2 + red_bytes + (st + 1) * 16 + kClusterXchBytes

@@ -118,10 +118,12 @@ def test_wide_rows_take_a_cluster(mode, rq):
     ("fp8", FP16, 32768, True, 1.0, 2, 8),
     ("fp8", FP16, 65536, False, 1.0, 2, 8),
     ("fp8", BF16, 65536, True, 1.0, 4, 8),
-    ("fp8", F32, 65536, True, 0.0, 16, 4),         # fp32 input keeps 4
+    ("fp8", F32, 65536, True, 0.0, 8, 8),          # fp32 FP8: two exchanges, one slot
+    ("fp8", F32, 32768, False, 0.0, 2, 8),
     ("nvfp4", BF16, 65536, True, 0.0, 8, 8),
     ("nvfp4", BF16, 131072, True, 0.0, 16, 8),
-    ("nvfp4", F32, 65536, True, 0.0, 16, 4),
+    ("nvfp4", F32, 65536, True, 0.0, 16, 8),
+    ("mxfp4", F32, 65536, True, 0.0, 16, 4),       # MXFP4 keeps 4 whatever the input
     ("mxfp4", BF16, 65536, True, 0.0, 8, 4),       # MXFP4 keeps 4
     ("mxfp4", BF16, 131072, True, 0.0, 16, 4),
     ("mxfp4", BF16, 131072, False, 0.0, 8, 8),     # 8 where 4 would take 512 threads
@@ -132,11 +134,10 @@ def test_cluster_sizes_and_vectors(mode, dtype, hidden, res, off, cluster, vpt, 
     assert (p["cluster"], p["vectors_per_thread"]) == (cluster, vpt), p
     nvc = hidden // (8 if dtype != F32 else 4) // cluster
     assert p["threads"] == ((nvc + vpt - 1) // vpt + 31) // 32 * 32
-    # pipelined kernels (one exchange per row) keep three slots; the two-exchange ones two,
-    # except the offset kernel with 16-bit input, which refills its one slot after the first
+    # pipelined kernels (one exchange per row) keep three slots; the FP8 kernels with two
+    # exchanges (an offset, or fp32 input) refill their one slot right after the first
     one_exchange = mode != "fp8" or (dtype != F32 and off == 0.0)
-    offset16 = mode == "fp8" and dtype != F32 and off != 0.0
-    assert p["stages"] == (3 if one_exchange else 1 if offset16 else 2)
+    assert p["stages"] == (3 if one_exchange else 1)
 
 
 def _widths(mode, dtype):
