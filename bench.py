@@ -854,6 +854,7 @@ def next_row_cases():
         ("NEXT-4", "cluster_rows_offset", W.config("fp8_gemma", rows=4096, hidden=65536), {}),
         ("NEXT-4", "cluster_rows_no_residual", W.Workload("wide_rows", "fp8", 4096, 65536, "bf16",
                                                           False, scale_ub=1200.0), {}),
+        ("NEXT-4", "fp32_input", wide("fp8", 2048, 65536), {"dtype": torch.float32}),
     ]
 
 
