@@ -63,7 +63,9 @@ def test_profiled_full_captures_are_the_planned_kernels(rq):
              "nvfp4_32768x7168_ncu_full.md": ("nvfp4", BF16, 7168, False, 0.0),
              "mxfp4_residual_65536x2048_ncu_full.md": ("mxfp4", BF16, 2048, True, 0.0),
              "cluster_fp8_4096x65536_ncu_full.md": ("fp8", BF16, 65536, True, 0.0),
-             "cluster_fp8_offset_4096x65536_ncu_full.md": ("fp8", FP16, 65536, True, 1.0)}
+             "cluster_fp8_offset_4096x65536_ncu_full.md": ("fp8", FP16, 65536, True, 1.0),
+             "cluster_fp8_fp32_2048x65536_ncu_full.md": ("fp8", F32, 65536, True, 0.0),
+             "cluster_fp8_2048x131072_ncu_full.md": ("fp8", BF16, 131072, True, 0.0)}
     for fn, (mode, dt, h, res, off) in cases.items():
         text = open(os.path.join(ROOT, "profiles", fn)).read()
         m = re.search(r"`void rmsq_row_kernel<([\d, ]+)>\(Params\)`", text)
