@@ -249,3 +249,11 @@ def test_argument_checks(rq):
     info = rq.PlanInfo()
     assert rq.lib().rmsq_plan(0, 0, 0, 0.0, 4096, 1024, 512, 0, ctypes.byref(info)) == 6
     assert rq.lib().rmsq_plan(0, 0, 0, 0.0, 4096, *rq.GB300_SMEM, None) == 1
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="a device is present")
+def test_device_limits_need_a_device(rq):
+    # smem=None asks for the current device's limits: without a GPU that is RMSQ_ERR_DEVICE
+    with pytest.raises(rq.RmsqError) as e:
+        rq.rmsq_plan("fp8", BF16, 4096, smem=None)
+    assert e.value.status == 7
