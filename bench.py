@@ -839,6 +839,7 @@ def next_row_cases():
         ("NEXT-2", "global_scale_prepass", nv, {"prepass": True}),
         ("NEXT-2", "global_scale_prepass", W.Workload("nvfp4_residual", "nvfp4", 8192, 4096,
                                                       "bf16", True), {"prepass": True}),
+        ("NEXT-2", "global_scale_prepass", wide("nvfp4", 4096, 65536), {"prepass": True}),
         ("NEXT-3", "fp32_input", f8, {"dtype": torch.float32}),
         ("NEXT-3", "fp32_input", W.config("mxfp4_residual", rows=4096, hidden=16384),
          {"dtype": torch.float32}),
